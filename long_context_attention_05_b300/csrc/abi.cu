@@ -1,0 +1,302 @@
+// Host side of the C ABI declared in include/csa.h: argument checks, workspace
+// layout, rotary phase tables and kernel launches.  No device memory is
+// allocated here; every buffer comes from the caller.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <algorithm>
+#include <cstring>
+#include <string>
+
+#include "kernels.h"
+
+namespace {
+
+thread_local std::string g_err;
+
+csa_status fail(csa_status s, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return s;
+}
+
+csa_status ok() {
+  g_err.clear();
+  return CSA_OK;
+}
+
+csa_status cuda_status(cudaError_t e, const char *what) {
+  if (e == cudaSuccess) return ok();
+  return fail(CSA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool a16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+long long entry_cap(const csa_cache *c) {
+  return c->page_size ? (long long)c->max_pages * c->page_size : (long long)c->max_entries;
+}
+
+csa_status check_cache(const csa_cache *c) {
+  if (!c) return fail(CSA_ERR_INVALID_ARG, "cache is NULL");
+  if (c->m < 1 || c->m > 1024) return fail(CSA_ERR_INVALID_ARG, "m=%d outside [1,1024]", c->m);
+  if (c->d_rope < 0 || c->d_rope > 64 || c->d_rope % 8 || c->d_rope > c->d)
+    return fail(CSA_ERR_INVALID_ARG, "d_rope=%d must be a multiple of 8 in [0,min(64,d)]", c->d_rope);
+  if (c->d < 16 || c->d % 16 || (c->d - c->d_rope) % 16)
+    return fail(CSA_ERR_INVALID_ARG, "d=%d: d and d-d_rope must be multiples of 16", c->d);
+  if (!(c->d_idx == 0 || c->d_idx == 16 || c->d_idx == 32 || c->d_idx == 64 || c->d_idx == 128))
+    return fail(CSA_ERR_UNSUPPORTED, "d_idx=%d not in {0,16,32,64,128}", c->d_idx);
+  if (c->d + c->d_idx > 1024) return fail(CSA_ERR_UNSUPPORTED, "d + d_idx = %d > 1024", c->d + c->d_idx);
+  if (c->kv_dtype != CSA_E4M3 && c->kv_dtype != CSA_F32)
+    return fail(CSA_ERR_INVALID_ARG, "kv_dtype must be CSA_E4M3 or CSA_F32");
+  if (c->win_dtype != CSA_BF16 && c->win_dtype != CSA_F32)
+    return fail(CSA_ERR_INVALID_ARG, "win_dtype must be CSA_BF16 or CSA_F32");
+  if (c->n_win < 1) return fail(CSA_ERR_INVALID_ARG, "n_win must be >= 1");
+  if (c->win_cap < c->n_win) return fail(CSA_ERR_INVALID_ARG, "win_cap=%d < n_win=%d", c->win_cap, c->n_win);
+  if (!(c->rope_theta > 1.0)) return fail(CSA_ERR_INVALID_ARG, "rope_theta must be > 1");
+  if (c->page_size < 0) return fail(CSA_ERR_INVALID_ARG, "page_size < 0");
+  if (c->page_size > 0) {
+    if (!c->page_table || c->max_pages < 1) return fail(CSA_ERR_INVALID_ARG, "paged cache needs page_table, max_pages");
+  } else if (c->max_entries < 1) {
+    return fail(CSA_ERR_INVALID_ARG, "max_entries must be >= 1");
+  }
+  if (!c->kv_nope || !c->kv_rope || !c->win || !c->pool_state || !c->n_tokens)
+    return fail(CSA_ERR_INVALID_ARG, "cache pointer is NULL");
+  if (c->kv_dtype == CSA_E4M3 && !c->kv_scale) return fail(CSA_ERR_INVALID_ARG, "kv_scale is NULL");
+  if (c->d_idx > 0 && (!c->idx_key || (c->kv_dtype == CSA_E4M3 && !c->idx_scale)))
+    return fail(CSA_ERR_INVALID_ARG, "indexer key pointers are NULL");
+  if (!a16(c->kv_nope) || !a16(c->kv_rope) || !a16(c->win) || !a16(c->pool_state) || !a16(c->idx_key) ||
+      ((uintptr_t)c->kv_scale & 3) || ((uintptr_t)c->idx_scale & 3) || ((uintptr_t)c->n_tokens & 7))
+    return fail(CSA_ERR_INVALID_ARG, "cache arrays must be 16-byte aligned");
+  return ok();
+}
+
+csa::CacheView view(const csa_cache *c) {
+  csa::CacheView v;
+  v.m = c->m; v.d = c->d; v.d_rope = c->d_rope; v.d_idx = c->d_idx; v.kv_dtype = c->kv_dtype;
+  v.win_dtype = c->win_dtype; v.n_win = c->n_win; v.win_cap = c->win_cap; v.page_size = c->page_size;
+  v.max_pages = c->max_pages; v.max_entries = c->max_entries; v.cap = entry_cap(c);
+  v.kv_nope = (const uint8_t *)c->kv_nope; v.kv_scale = c->kv_scale; v.kv_rope = (const uint8_t *)c->kv_rope;
+  v.idx_key = (const uint8_t *)c->idx_key; v.idx_scale = c->idx_scale; v.page_table = c->page_table;
+  v.win = (const uint8_t *)c->win; v.pool_state = c->pool_state; v.n_tokens = (long long *)c->n_tokens;
+  return v;
+}
+
+// Fixed-point phase increment per rotary frequency: round(2^64 * f_i / (2 pi)),
+// f_i = theta^(-2i/d_rope), evaluated in x87 extended precision.
+csa::RopeTable rope_table(double theta, int d_rope) {
+  thread_local double last_theta = -1;
+  thread_local int last_dr = -1;
+  thread_local csa::RopeTable tab;
+  if (theta == last_theta && d_rope == last_dr) return tab;
+  std::memset(&tab, 0, sizeof(tab));
+  const long double two_pi = 6.283185307179586476925286766559005768L;
+  for (int i = 0; i < d_rope / 2; ++i) {
+    const long double f = powl((long double)theta, -2.0L * i / (long double)d_rope);
+    const long double turns = f / two_pi;                       // in (0, 1)
+    tab.step[i] = (unsigned long long)llroundl(ldexpl(turns, 64));   // < 2^62
+  }
+  last_theta = theta;
+  last_dr = d_rope;
+  return tab;
+}
+
+[[maybe_unused]] int num_sms() {
+  thread_local int dev = -1, n = 148;
+  int cur = 0;
+  if (cudaGetDevice(&cur) != cudaSuccess) return n;
+  if (cur != dev) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, cur) == cudaSuccess && v > 0) n = v;
+    dev = cur;
+  }
+  return n;
+}
+
+constexpr size_t kHeader = 256;
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct AttendPlan {
+  int n_splits, cps;
+  size_t part_o_bytes, part_ml_bytes;
+};
+
+AttendPlan attend_plan(const csa_cache *c, int batch, int n_q, int heads, long long list_cap) {
+  AttendPlan p;
+  csa::attend_plan(n_q, list_cap, c->n_win, p.n_splits, p.cps);
+  const size_t parts = (size_t)batch * n_q * p.n_splits * heads;
+  p.part_o_bytes = p.n_splits > 1 ? align256(parts * c->d * sizeof(float)) : 0;
+  p.part_ml_bytes = p.n_splits > 1 ? align256(parts * 2 * sizeof(float)) : 0;
+  return p;
+}
+
+size_t scores_bytes(const csa_cache *c, int batch, int n_q) {
+  return align256((size_t)batch * n_q * entry_cap(c) * sizeof(float));
+}
+
+csa_status check_ws(void *ws, size_t ws_bytes, size_t need) {
+  if (need == 0) return ok();
+  if (!ws) return fail(CSA_ERR_WORKSPACE, "workspace is NULL (need %zu bytes)", need);
+  if (((uintptr_t)ws & 255u)) return fail(CSA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (ws_bytes < need) return fail(CSA_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, need);
+  return ok();
+}
+
+csa_status check_q(int batch, int n_q, const csa_cache *c) {
+  if (batch < 1 || n_q < 1) return fail(CSA_ERR_INVALID_ARG, "batch=%d n_q=%d must be >= 1", batch, n_q);
+  if ((long long)c->win_cap < (long long)c->n_win + n_q - 1)
+    return fail(CSA_ERR_INVALID_ARG, "win_cap=%d < n_win + n_q - 1 = %d", c->win_cap, c->n_win + n_q - 1);
+  return ok();
+}
+
+csa_status attend_common(const csa_cache *c, int batch, int n_q, const void *q, int q_dtype, int heads,
+                         const float *sink, const int32_t *idx, int k, void *out, int out_dtype, float *out_lse,
+                         void *ws, size_t ws_bytes, cudaStream_t st) {
+  csa_status s = check_cache(c);
+  if (s) return s;
+  if ((s = check_q(batch, n_q, c))) return s;
+  if (heads < 1 || heads > 128) return fail(CSA_ERR_UNSUPPORTED, "heads=%d outside [1,128]", heads);
+  if (!q || !sink || !out) return fail(CSA_ERR_INVALID_ARG, "q, sink and out must be non-NULL");
+  if (q_dtype != CSA_BF16 && q_dtype != CSA_F32) return fail(CSA_ERR_INVALID_ARG, "q_dtype must be BF16 or F32");
+  if (out_dtype != CSA_BF16 && out_dtype != CSA_F32) return fail(CSA_ERR_INVALID_ARG, "out_dtype must be BF16 or F32");
+  if (idx && k < 1) return fail(CSA_ERR_INVALID_ARG, "k must be >= 1");
+  if (csa::attend_smem_bytes(c->d) > 227 * 1024) return fail(CSA_ERR_UNSUPPORTED, "d=%d too large", c->d);
+  const long long list_cap = idx ? (long long)k : entry_cap(c);
+  const AttendPlan p = attend_plan(c, batch, n_q, heads, list_cap);
+  const size_t need = p.n_splits > 1 ? kHeader + p.part_o_bytes + p.part_ml_bytes : 0;
+  if ((s = check_ws(ws, ws_bytes, need))) return s;
+  csa::AttendArgs a;
+  a.c = view(c);
+  a.rope = rope_table(c->rope_theta, c->d_rope);
+  a.n_q = n_q; a.heads = heads; a.q_dtype = q_dtype; a.out_dtype = out_dtype;
+  a.q = (const uint8_t *)q; a.sink = sink; a.idx = idx; a.k = k;
+  a.n_splits = p.n_splits; a.chunks_per_split = p.cps;
+  a.part_o = need ? (float *)((char *)ws + kHeader) : nullptr;
+  a.part_ml = need ? (float *)((char *)ws + kHeader + p.part_o_bytes) : nullptr;
+  a.out = (uint8_t *)out; a.out_lse = out_lse;
+  a.scale = (float)(1.0 / std::sqrt((double)c->d));
+  return cuda_status(csa::launch_attend(a, batch * n_q, st), "attention launch");
+}
+
+csa_status check_index_args(const csa_cache *c, int batch, int n_q, const void *q_idx, int q_dtype, const float *w,
+                            int heads_idx) {
+  csa_status s = check_cache(c);
+  if (s) return s;
+  if ((s = check_q(batch, n_q, c))) return s;
+  if (c->d_idx == 0) return fail(CSA_ERR_INVALID_ARG, "cache has no indexer stream (d_idx == 0)");
+  if (heads_idx < 1 || heads_idx > 128) return fail(CSA_ERR_UNSUPPORTED, "heads_idx=%d outside [1,128]", heads_idx);
+  if (!q_idx || !w) return fail(CSA_ERR_INVALID_ARG, "q_idx and w must be non-NULL");
+  if (q_dtype != CSA_BF16 && q_dtype != CSA_F32) return fail(CSA_ERR_INVALID_ARG, "q_dtype must be BF16 or F32");
+  if ((size_t)heads_idx * (c->d_idx + 1) * sizeof(float) > 227 * 1024)
+    return fail(CSA_ERR_UNSUPPORTED, "indexer query too large");
+  return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+int csa_version(void) { return 100; }
+
+const char *csa_last_error(void) { return g_err.c_str(); }
+
+size_t csa_workspace_size(const csa_cache *c, int batch, int n_q, int heads, int k) {
+  if (check_cache(c) || batch < 1 || n_q < 1 || heads < 1) return 0;
+  size_t need = kHeader;
+  if (k > 0) need = std::max(need, kHeader + scores_bytes(c, batch, n_q));
+  const AttendPlan p = attend_plan(c, batch, n_q, heads, k > 0 ? (long long)k : entry_cap(c));
+  need = std::max(need, kHeader + p.part_o_bytes + p.part_ml_bytes);
+  return need;
+}
+
+csa_status csa_compress(const csa_cache *c, int batch, int n_new, const void *x, const void *gate, const void *idx_x,
+                        const void *idx_gate, const float *pos_bias, const float *idx_pos_bias, int in_dtype,
+                        csa_stream_t stream) {
+  csa_status s = check_cache(c);
+  if (s) return s;
+  if (batch < 1 || n_new < 1) return fail(CSA_ERR_INVALID_ARG, "batch=%d n_new=%d must be >= 1", batch, n_new);
+  if (in_dtype != c->win_dtype) return fail(CSA_ERR_INVALID_ARG, "in_dtype must equal the ring dtype");
+  if (!x || !gate || !pos_bias) return fail(CSA_ERR_INVALID_ARG, "x, gate and pos_bias must be non-NULL");
+  if (c->d_idx > 0 && (!idx_x || !idx_gate || !idx_pos_bias))
+    return fail(CSA_ERR_INVALID_ARG, "indexer-key inputs must be non-NULL when d_idx > 0");
+  return cuda_status(csa::launch_compress(view(c), rope_table(c->rope_theta, c->d_rope), batch, n_new, in_dtype, x,
+                                          gate, idx_x, idx_gate, pos_bias, idx_pos_bias, (cudaStream_t)stream),
+                     "compress launch");
+}
+
+csa_status csa_index_scores(const csa_cache *c, int batch, int n_q, const void *q_idx, int q_dtype, const float *w,
+                            int heads_idx, float *scores, int64_t stride, void *ws, size_t ws_bytes,
+                            csa_stream_t stream) {
+  (void)ws; (void)ws_bytes;
+  csa_status s = check_index_args(c, batch, n_q, q_idx, q_dtype, w, heads_idx);
+  if (s) return s;
+  if (!scores) return fail(CSA_ERR_INVALID_ARG, "scores is NULL");
+  if (stride < entry_cap(c)) return fail(CSA_ERR_INVALID_ARG, "scores_stride %lld < entry capacity %lld",
+                                         (long long)stride, entry_cap(c));
+  return cuda_status(csa::launch_index_generic(view(c), batch, n_q, q_idx, q_dtype, w, heads_idx, scores, stride,
+                                               entry_cap(c), (cudaStream_t)stream),
+                     "indexer launch");
+}
+
+csa_status csa_topk(const csa_cache *c, int batch, int n_q, const float *scores, int64_t stride, int k,
+                    int32_t *out_idx, int32_t *out_count, void *ws, size_t ws_bytes, csa_stream_t stream) {
+  (void)ws; (void)ws_bytes;
+  csa_status s = check_cache(c);
+  if (s) return s;
+  if (batch < 1 || n_q < 1) return fail(CSA_ERR_INVALID_ARG, "batch and n_q must be >= 1");
+  if (k < 1) return fail(CSA_ERR_INVALID_ARG, "k must be >= 1");
+  if (!scores || !out_idx || !out_count) return fail(CSA_ERR_INVALID_ARG, "NULL pointer");
+  if (stride < 1) return fail(CSA_ERR_INVALID_ARG, "scores_stride must be >= 1");
+  return cuda_status(csa::launch_topk(view(c), batch, n_q, scores, stride, k, out_idx, out_count,
+                                      (cudaStream_t)stream),
+                     "top-k launch");
+}
+
+csa_status csa_index_topk(const csa_cache *c, int batch, int n_q, const void *q_idx, int q_dtype, const float *w,
+                          int heads_idx, int k, int32_t *out_idx, int32_t *out_count, void *ws, size_t ws_bytes,
+                          csa_stream_t stream) {
+  csa_status s = check_index_args(c, batch, n_q, q_idx, q_dtype, w, heads_idx);
+  if (s) return s;
+  if (k < 1) return fail(CSA_ERR_INVALID_ARG, "k must be >= 1");
+  if (!out_idx || !out_count) return fail(CSA_ERR_INVALID_ARG, "NULL output pointer");
+  const size_t need = kHeader + scores_bytes(c, batch, n_q);
+  if ((s = check_ws(ws, ws_bytes, need))) return s;
+  float *scores = (float *)((char *)ws + kHeader);
+  const long long cap = entry_cap(c);
+  cudaError_t e = csa::launch_index_generic(view(c), batch, n_q, q_idx, q_dtype, w, heads_idx, scores, cap, cap,
+                                            (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_status(e, "indexer launch");
+  return cuda_status(csa::launch_topk(view(c), batch, n_q, scores, cap, k, out_idx, out_count, (cudaStream_t)stream),
+                     "top-k launch");
+}
+
+csa_status csa_sparse_attend(const csa_cache *c, int batch, int n_q, const void *q, int q_dtype, int heads,
+                             const float *sink, const int32_t *idx, int k, void *out, int out_dtype, float *out_lse,
+                             void *ws, size_t ws_bytes, csa_stream_t stream) {
+  if (!idx) return fail(CSA_ERR_INVALID_ARG, "idx is NULL");
+  return attend_common(c, batch, n_q, q, q_dtype, heads, sink, idx, k, out, out_dtype, out_lse, ws, ws_bytes,
+                       (cudaStream_t)stream);
+}
+
+csa_status hca_attend(const csa_cache *c, int batch, int n_q, const void *q, int q_dtype, int heads,
+                      const float *sink, void *out, int out_dtype, float *out_lse, void *ws, size_t ws_bytes,
+                      csa_stream_t stream) {
+  return attend_common(c, batch, n_q, q, q_dtype, heads, sink, nullptr, 0, out, out_dtype, out_lse, ws, ws_bytes,
+                       (cudaStream_t)stream);
+}
+
+csa_status csa_device_status(void *ws, int *status, csa_stream_t stream) {
+  if (!ws || !status) return fail(CSA_ERR_INVALID_ARG, "NULL pointer");
+  int v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, ws, sizeof(int), cudaMemcpyDeviceToHost, (cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws, 0, sizeof(int), (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_status(e, "device status read");
+  *status = v;
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,38 @@
+// Host-side declarations of the kernel launchers (one translation unit each).
+#pragma once
+#include "common.cuh"
+
+namespace csa {
+
+cudaError_t launch_compress(const CacheView &c, const RopeTable &rope, int batch, int n_new, int in_dtype,
+                            const void *x, const void *gate, const void *ix, const void *ig,
+                            const float *pb, const float *ipb, cudaStream_t st);
+
+cudaError_t launch_index_generic(const CacheView &c, int batch, int n_q, const void *q_idx, int q_dtype,
+                                 const float *w, int heads_idx, float *scores, long long stride,
+                                 long long n_cap, cudaStream_t st);
+
+cudaError_t launch_topk(const CacheView &c, int batch, int n_q, const float *scores, long long stride, int k,
+                        int32_t *out_idx, int32_t *out_count, cudaStream_t st);
+
+constexpr int kHG = 16;
+constexpr int kKC = 32;
+struct AttendArgs {
+  CacheView c;
+  RopeTable rope;
+  int n_q, heads, q_dtype, out_dtype;
+  const uint8_t *q;
+  const float *sink;
+  const int32_t *idx;   // nullptr: dense (HCA)
+  int k;
+  int n_splits, chunks_per_split;
+  float *part_o, *part_ml;
+  uint8_t *out;
+  float *out_lse;
+  float scale;          // 1/sqrt(d)
+};
+void attend_plan(int n_q, long long list_cap, int n_win, int &n_splits, int &cps);
+size_t attend_smem_bytes(int d);
+cudaError_t launch_attend(const AttendArgs &a, int rows, cudaStream_t st);
+
+}  // namespace csa

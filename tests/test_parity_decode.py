@@ -1,0 +1,158 @@
+"""GPU vs oracle parity of the decode path (compress one token, indexer, top-k,
+sparse / dense attention) on the seeded workloads, through the C ABI.
+
+Tolerances: fp32 mode 1e-5 and bf16/e4m3 mode 2e-3 of the row's largest
+|oracle value| (bf16 outputs additionally get half a bf16 ulp of the oracle
+value: the output format's own rounding).  Top-k sets must match exactly except
+for near-ties within 1e-6 relative of the k-th score, which are counted.
+"""
+import numpy as np
+import pytest
+import torch
+
+import harness as H
+import long_context_attention_05_b300 as L
+from long_context_attention_05_b300 import synthetic as S
+from oracle import csa_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_step(w, arrs, inp, res, tol, rows=None, what="", out_bf16=None):
+    """Compares GPU results of a seeded step with the oracle for the given
+    (b, i) query rows (all rows by default).  Returns the tie count."""
+    out_bf16 = (w.tok_dtype != "f32") if out_bf16 is None else out_bf16
+    rows = rows if rows is not None else [(b, i) for b in range(w.batch) for i in range(w.n_new)]
+    ties = 0
+    ent_cache = {}
+    redo = []
+    for b, i in rows:
+        ref = H.oracle_seeded_step(w, arrs, inp, b, i, ent_cache=ent_cache)
+        tag = f"{what} b={b} i={i}"
+        if w.kind == "csa":
+            r = b * w.n_new + i
+            if "scores" in res:
+                H.check_rows(res["scores"][r, : ref["n_vis"]][None], ref["scores"][None],
+                             tol if w.kv_dtype == "f32" else 1e-5, what=tag + " scores", extra=ref["slack"][None])
+            nt = H.check_topk(res["idx"][b, i], res["cnt"][b, i], ref["idx"], ref["count"], ref["scores"], tag,
+                              slack=ref["slack"])
+            ties += nt
+            if nt:
+                redo.append((b, i, ref))
+                continue
+        H.check_rows(res["o"][b, i], ref["o"], tol, out_bf16=out_bf16, what=tag + " out")
+        assert np.all(np.abs(res["lse"][b, i] - ref["lse"]) <= tol * np.maximum(1, np.abs(ref["lse"]))), tag + " lse"
+    if redo:
+        # near-tie flips: check attention on the oracle's own index set
+        idx = torch.from_numpy(res["idx"]).cuda()
+        for b, i, ref in redo:
+            idx[b, i] = torch.from_numpy(ref["idx"]).cuda()
+        out = torch.empty_like(res["gi"]["q"], dtype=torch.float32 if not out_bf16 else torch.bfloat16)
+        lse = torch.empty((w.batch, w.n_new, w.heads), dtype=torch.float32, device="cuda")
+        L.csa_sparse_attend(res["cache"], res["gi"]["q"], res["gi"]["sink"], idx, out, lse, res["ws"])
+        o = out.float().cpu().numpy()
+        for b, i, ref in redo:
+            H.check_rows(o[b, i], ref["o"], tol, out_bf16=out_bf16, what=f"{what} b={b} i={i} out(oracle idx)")
+    return ties
+
+
+def _seeded(w):
+    inp = S.step_inputs(w)
+    arrs = S.seeded_cache(w, inp.get("q_idx"), inp.get("w_idx"))
+    return arrs, inp
+
+
+# ----------------------------------------------------------------------------- config 0 (fp32, compressor-built)
+def test_c0_csa_decode_fp32_built_by_compressor():
+    w = S.config0()
+    ctx = S.context_tokens(w)
+    inp = S.step_inputs(w)
+    cache = L.Cache.from_host(w, S.empty_cache(w))
+    gi = H.gpu_inputs(w, inp)
+    gc = {k: L.to_device(v) for k, v in ctx.items()}
+    L.csa_compress(cache, gc["x"], gc["gate"], gi["pos_bias"], gc["idx_x"], gc["idx_gate"], gi["idx_pos_bias"])
+    H.gpu_compress(w, cache, gi)            # token 4095 completes block 1023
+    ws = L.alloc_workspace(cache, 1, 1, w.heads, w.k)
+    res = H.gpu_query_stages(w, cache, gi, torch.float32, ws)
+    assert int(cache.t["n_tokens"][0]) == 4096
+
+    x = np.concatenate([ctx["x"][0], inp["x"][0]]).astype(np.float64)
+    g = np.concatenate([ctx["gate"][0], inp["gate"][0]]).astype(np.float64)
+    ix = np.concatenate([ctx["idx_x"][0], inp["idx_x"][0]]).astype(np.float64)
+    ig = np.concatenate([ctx["idx_gate"][0], inp["idx_gate"][0]]).astype(np.float64)
+    st = O.compress_entries(x, g, inp["pos_bias"], 4, 64, w.theta, "f32", 0, 1024)
+    ks = O.compress_index_keys(ix, ig, inp["idx_pos_bias"], 4, "f32", 0, 1024)
+    # stored entries and indexer keys
+    H.check_rows(cache.t["kv_nope"][:1024].cpu().numpy(), st["kv_nope"], H.TOL_F32, what="kv_nope")
+    H.check_rows(cache.t["kv_rope"][:1024].cpu().numpy(), st["kv_rope"], H.TOL_F32, what="kv_rope")
+    H.check_rows(cache.t["idx_key"][:1024].cpu().numpy(), ks["idx_key"], H.TOL_F32, what="idx_key")
+    # window ring holds the last raw tokens exactly
+    ring = cache.t["win"][0].cpu().numpy()
+    for p in range(4096 - 128, 4096):
+        assert np.array_equal(ring[p % w.win_cap], x[p].astype(np.float32))
+    ent = O.decode_kv(st["kv_nope"], None, st["kv_rope"], "f32")
+    keys = O.decode_index_keys(ks["idx_key"], None, "f32")
+    ref = O.query_step("csa", inp["q"][0, 0].astype(np.float64), 4095, inp["sink"].astype(np.float64), ent,
+                       lambda pos: x[pos], 4, 128, 64, w.theta, q_idx=inp["q_idx"][0, 0].astype(np.float64),
+                       w_idx=inp["w_idx"][0, 0].astype(np.float64), idx_keys=keys, k=64)
+    H.check_rows(res["scores"][0, :1024][None], ref["scores"][None], H.TOL_F32, what="scores")
+    assert H.check_topk(res["idx"][0, 0], res["cnt"][0, 0], ref["idx"], ref["count"], ref["scores"], "topk") == 0
+    H.check_rows(res["o"][0, 0], ref["o"], H.TOL_F32, what="out")
+    assert np.allclose(res["lse"][0, 0], ref["lse"], rtol=0, atol=H.TOL_F32)
+
+
+def test_c0_chained_index_topk_matches_separate_calls():
+    w = S.config0(ctx=(1024,), seeded_cache=True)
+    arrs, inp = _seeded(w)
+    a = H.gpu_seeded_step(w, arrs, inp, torch.float32, chained=False)
+    b = H.gpu_seeded_step(w, arrs, inp, torch.float32, chained=True)
+    assert np.array_equal(a["idx"], b["idx"]) and np.array_equal(a["cnt"], b["cnt"])
+    assert np.array_equal(a["o"], b["o"])
+
+
+# ----------------------------------------------------------------------------- config 1 (HCA)
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_c1_hca_decode(out):
+    w = S.config1()
+    arrs, inp = _seeded(w)
+    res = H.gpu_seeded_step(w, arrs, inp, torch.bfloat16 if out == "bf16" else torch.float32)
+    _check_step(w, arrs, inp, res, H.TOL_LOW, what="c1", out_bf16=(out == "bf16"))
+
+
+# ----------------------------------------------------------------------------- config 2 (CSA 1M)
+@pytest.mark.parametrize("ctx", [4096, 65536])
+def test_c2_geometry_small_contexts(ctx):
+    w = S.config2(ctx=(ctx, ctx + 512, ctx + 1024, ctx + 4096))
+    arrs, inp = _seeded(w)
+    res = H.gpu_seeded_step(w, arrs, inp)
+    _check_step(w, arrs, inp, res, H.TOL_LOW, what=f"c2@{ctx}")
+    res32 = H.gpu_seeded_step(w, arrs, inp, torch.float32)
+    _check_step(w, arrs, inp, res32, H.TOL_LOW, what=f"c2@{ctx} f32", out_bf16=False)
+
+
+def test_c2_full_1m_context():
+    w = S.config2()
+    arrs, inp = _seeded(w)
+    res = H.gpu_seeded_step(w, arrs, inp)
+    ties = _check_step(w, arrs, inp, res, H.TOL_LOW, what="c2 full")
+    print(f"c2 full: near-tie flips {ties}")
+    # planted entries dominate the selection
+    for b in range(w.batch):
+        assert res["cnt"][b, 0] == w.k
+
+
+def test_c2_fewer_visible_entries_than_k():
+    w = S.config2(ctx=(4096, 8192, 12, 4), k=2048)    # 1024, 2048, 3 and 1 visible entries
+    arrs, inp = _seeded(w)
+    res = H.gpu_seeded_step(w, arrs, inp)
+    _check_step(w, arrs, inp, res, H.TOL_LOW, what="c2 short")
+    assert list(res["cnt"][:, 0]) == [1024, 2048, 3, 1]
+
+
+# ----------------------------------------------------------------------------- config 4 (paged hybrid stack)
+def test_c4_stack_small_paged():
+    ctx = (8192, 12800, 20480, 9088, 8320)
+    for w in S.config4_layers(ctx=ctx):
+        arrs, inp = _seeded(w)
+        res = H.gpu_seeded_step(w, arrs, inp)
+        _check_step(w, arrs, inp, res, H.TOL_LOW, what=w.name)
