@@ -122,52 +122,77 @@ def _alg_bytes(w):
     return idx_bytes, idx_bytes + att + q_bytes + out_bytes + new_tok + win
 
 
-def _oracle_rows(wl, budget_s):
-    from threadpoolctl import threadpool_limits
+def _oracle_rows_inproc(workload, budget_s, n_layers, steps=1, warmup=0):
+    """Times the oracle on whole query rows (one sequence's query at a time):
+    `warmup` untimed rows, then `steps` sample steps of at least one row each,
+    together about budget_s seconds.  Inputs are generated once."""
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     import harness as H
     from long_context_attention_05_b300 import synthetic as S
-    n_rows, t_total, per_layer = 0, 0.0, []
-    with threadpool_limits(limits=1):
-        for w in wl:
-            inp = S.step_inputs(w)
-            arrs = S.seeded_cache(w, inp.get("q_idx"), inp.get("w_idx"))
-            for b in range(w.batch):
-                t0 = time.perf_counter()
-                H.oracle_seeded_step(w, arrs, inp, b, 0)
-                dt = time.perf_counter() - t0
-                t_total += dt
-                n_rows += 1
-                per_layer.append((w.name, dt))
-                if t_total >= budget_s:
-                    break
-            if t_total >= budget_s:
+    wl = _workload(workload, 0)[:n_layers]
+    data = []
+    for w in wl:
+        inp = S.step_inputs(w)
+        arrs = S.seeded_cache(w, inp.get("q_idx"), inp.get("w_idx"))
+        rows = [(b, 0) for b in range(w.batch)] if w.mode == "decode" else [(0, i) for i in range(w.n_new)]
+        data.append((w, inp, arrs, rows))
+    order = [(li, r) for r in range(max(len(d[3]) for d in data)) for li in range(len(data)) if r < len(data[li][3])]
+    pos = 0
+
+    def one_row():
+        nonlocal pos
+        li, r = order[pos % len(order)]
+        pos += 1
+        w, inp, arrs, rows = data[li]
+        b, i = rows[r]
+        t0 = time.perf_counter()
+        H.oracle_seeded_step(w, arrs, inp, b, i)
+        return time.perf_counter() - t0
+
+    for _ in range(warmup):
+        one_row()
+    per_step = budget_s / max(steps, 1)
+    n_rows, t_total = 0, 0.0
+    for _ in range(steps):
+        t_step = 0.0
+        while True:
+            t_step += one_row()
+            n_rows += 1
+            if t_step >= per_step:
                 break
-            del arrs
-    return n_rows, t_total, per_layer
+        t_total += t_step
+    return n_rows, t_total
+
+
+def _oracle_rows(workload, budget_s, n_layers=1, steps=1, warmup=0):
+    """Runs the oracle sample in a fresh single-threaded process (BLAS and OpenMP
+    pinned to one thread; spawned, never forked from a CUDA process)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               NUMEXPR_NUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-sample", workload, str(budget_s),
+                        str(n_layers), str(steps), str(warmup)], capture_output=True, text=True, env=env)
+    if r.returncode != 0:
+        raise RuntimeError("oracle sample failed:\n" + r.stderr[-2000:])
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    return d["rows"], d["seconds"]
 
 
 def run_reference(args):
     wl = _workload(args.workload, 0)
-    if args.workload == "stack_decode_paged":
-        wl = wl[:2]
-    rows_total, t_total = 0, 0.0
-    for _ in range(args.warmup):
-        _oracle_rows(wl[:1], 0.0)
-    for _ in range(args.steps):
-        n, t, _ = _oracle_rows(wl, args.budget / max(args.steps, 1))
-        rows_total += n
-        t_total += t
+    n_layers = 2 if args.workload == "stack_decode_paged" else 1
+    per_step = args.budget / max(args.steps, 1)
+    rows_total, t_total = _oracle_rows(args.workload, args.budget, n_layers, args.steps, args.warmup)
     qps = rows_total / t_total
-    # a query of the stack is one row in each of its 4 layers
-    if args.workload == "stack_decode_paged":
+    if n_layers == 2:   # a query of the stack is one row in each of its 4 layers (2 CSA, 2 HCA)
         qps /= 2.0
-    sample = f"{rows_total} oracle query rows of {args.workload} (fp64 numpy, 1 thread)"
+    sample = (f"{rows_total} oracle query rows of {wl[0].name} (fp64 numpy, 1 thread, "
+              f"{args.steps} steps of >= 1 row and ~{per_step:.2f} s)")
     line = {"metric": "CSA/HCA decode queries/s at 1M ctx; achieved HBM GB/s vs B300 peak", "value": qps,
             "unit": "queries/s", "impl": "reference", "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1000.0 * t_total / max(args.steps, 1),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic (seeded)", "config": {"workload": wl[0].name},
+            "data": "synthetic (seeded caches, no weights)",
+            "config": {"workload": wl[0].name if n_layers == 1 else args.workload},
             "cpu_baseline": {"value": qps, "unit": "queries/s", "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": qps, "unit": "queries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -292,8 +317,9 @@ def run_ours(args, rank, world, local_rank):
         return
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        n, t, _ = _oracle_rows(wl[:1] if args.workload != "stack_decode_paged" else wl[:2], args.budget)
-        qps = n / t / (2.0 if args.workload == "stack_decode_paged" else 1.0)
+        nl = 2 if args.workload == "stack_decode_paged" else 1
+        n, t = _oracle_rows(args.workload, args.budget, nl)
+        qps = n / t / float(nl)
         cpu = {"value": qps, "unit": "queries/s", "cores": 1, "kind": "oracle",
                "sample": f"{n} oracle query rows of {w0l.name} (fp64 numpy, 1 thread), {t:.1f} s"}
     gqa8 = 8 * 128 * 2 * 2
@@ -321,6 +347,11 @@ def run_ours(args, rank, world, local_rank):
 
 
 def main():
+    if len(sys.argv) > 1 and sys.argv[1] == "--oracle-sample":
+        n, t = _oracle_rows_inproc(sys.argv[2], float(sys.argv[3]), int(sys.argv[4]), int(sys.argv[5]),
+                                   int(sys.argv[6]))
+        print(json.dumps({"rows": n, "seconds": t}))
+        return
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)

@@ -104,7 +104,7 @@ csa::RopeTable rope_table(double theta, int d_rope) {
   return tab;
 }
 
-[[maybe_unused]] int num_sms() {
+int num_sms() {
   thread_local int dev = -1, n = 148;
   int cur = 0;
   if (cudaGetDevice(&cur) != cudaSuccess) return n;
@@ -120,13 +120,15 @@ constexpr size_t kHeader = 256;
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct AttendPlan {
+  bool tc;
   int n_splits, cps;
   size_t part_o_bytes, part_ml_bytes;
 };
 
 AttendPlan attend_plan(const csa_cache *c, int batch, int n_q, int heads, long long list_cap) {
   AttendPlan p;
-  csa::attend_plan(n_q, list_cap, c->n_win, p.n_splits, p.cps);
+  p.tc = csa::attend_tc_supported(view(c), heads, CSA_BF16);
+  csa::attend_plan(n_q, list_cap, c->n_win, p.tc, p.n_splits, p.cps);
   const size_t parts = (size_t)batch * n_q * p.n_splits * heads;
   p.part_o_bytes = p.n_splits > 1 ? align256(parts * c->d * sizeof(float)) : 0;
   p.part_ml_bytes = p.n_splits > 1 ? align256(parts * 2 * sizeof(float)) : 0;
@@ -178,7 +180,8 @@ csa_status attend_common(const csa_cache *c, int batch, int n_q, const void *q, 
   a.part_ml = need ? (float *)((char *)ws + kHeader + p.part_o_bytes) : nullptr;
   a.out = (uint8_t *)out; a.out_lse = out_lse;
   a.scale = (float)(1.0 / std::sqrt((double)c->d));
-  return cuda_status(csa::launch_attend(a, batch * n_q, st), "attention launch");
+  return cuda_status(p.tc ? csa::launch_attend_tc(a, batch * n_q, st) : csa::launch_attend(a, batch * n_q, st),
+                     "attention launch");
 }
 
 csa_status check_index_args(const csa_cache *c, int batch, int n_q, const void *q_idx, int q_dtype, const float *w,
@@ -193,6 +196,17 @@ csa_status check_index_args(const csa_cache *c, int batch, int n_q, const void *
   if ((size_t)heads_idx * (c->d_idx + 1) * sizeof(float) > 227 * 1024)
     return fail(CSA_ERR_UNSUPPORTED, "indexer query too large");
   return ok();
+}
+
+// Indexer dispatch: the tensor-core kernel for e4m3 keys of dim 128 and 32/64/128
+// heads; the CUDA-core kernel otherwise (fp32 caches, other dims).
+cudaError_t launch_indexer(const csa_cache *c, int batch, int n_q, const void *q_idx, int q_dtype, const float *w,
+                           int heads_idx, float *scores, long long stride, void *ws, cudaStream_t st) {
+  const csa::CacheView v = view(c);
+  if (csa::index_tc_supported(v, heads_idx))
+    return csa::launch_index_tc(v, batch, n_q, q_idx, q_dtype, w, heads_idx, scores, stride, num_sms(),
+                                ws ? (int *)ws : nullptr, st);
+  return csa::launch_index_generic(v, batch, n_q, q_idx, q_dtype, w, heads_idx, scores, stride, entry_cap(c), st);
 }
 
 }  // namespace
@@ -230,14 +244,15 @@ csa_status csa_compress(const csa_cache *c, int batch, int n_new, const void *x,
 csa_status csa_index_scores(const csa_cache *c, int batch, int n_q, const void *q_idx, int q_dtype, const float *w,
                             int heads_idx, float *scores, int64_t stride, void *ws, size_t ws_bytes,
                             csa_stream_t stream) {
-  (void)ws; (void)ws_bytes;
   csa_status s = check_index_args(c, batch, n_q, q_idx, q_dtype, w, heads_idx);
   if (s) return s;
   if (!scores) return fail(CSA_ERR_INVALID_ARG, "scores is NULL");
   if (stride < entry_cap(c)) return fail(CSA_ERR_INVALID_ARG, "scores_stride %lld < entry capacity %lld",
                                          (long long)stride, entry_cap(c));
-  return cuda_status(csa::launch_index_generic(view(c), batch, n_q, q_idx, q_dtype, w, heads_idx, scores, stride,
-                                               entry_cap(c), (cudaStream_t)stream),
+  if (ws && ((uintptr_t)ws & 255u)) return fail(CSA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (ws && ws_bytes < kHeader) return fail(CSA_ERR_WORKSPACE, "workspace smaller than its %zu-byte header", kHeader);
+  return cuda_status(launch_indexer(c, batch, n_q, q_idx, q_dtype, w, heads_idx, scores, stride, ws,
+                                    (cudaStream_t)stream),
                      "indexer launch");
 }
 
@@ -250,7 +265,7 @@ csa_status csa_topk(const csa_cache *c, int batch, int n_q, const float *scores,
   if (k < 1) return fail(CSA_ERR_INVALID_ARG, "k must be >= 1");
   if (!scores || !out_idx || !out_count) return fail(CSA_ERR_INVALID_ARG, "NULL pointer");
   if (stride < 1) return fail(CSA_ERR_INVALID_ARG, "scores_stride must be >= 1");
-  return cuda_status(csa::launch_topk(view(c), batch, n_q, scores, stride, k, out_idx, out_count,
+  return cuda_status(csa::launch_topk(view(c), batch, n_q, scores, stride, k, out_idx, out_count, num_sms(),
                                       (cudaStream_t)stream),
                      "top-k launch");
 }
@@ -266,10 +281,9 @@ csa_status csa_index_topk(const csa_cache *c, int batch, int n_q, const void *q_
   if ((s = check_ws(ws, ws_bytes, need))) return s;
   float *scores = (float *)((char *)ws + kHeader);
   const long long cap = entry_cap(c);
-  cudaError_t e = csa::launch_index_generic(view(c), batch, n_q, q_idx, q_dtype, w, heads_idx, scores, cap, cap,
-                                            (cudaStream_t)stream);
+  cudaError_t e = launch_indexer(c, batch, n_q, q_idx, q_dtype, w, heads_idx, scores, cap, ws, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_status(e, "indexer launch");
-  return cuda_status(csa::launch_topk(view(c), batch, n_q, scores, cap, k, out_idx, out_count, (cudaStream_t)stream),
+  return cuda_status(csa::launch_topk(view(c), batch, n_q, scores, cap, k, out_idx, out_count, num_sms(), (cudaStream_t)stream),
                      "top-k launch");
 }
 

@@ -228,14 +228,15 @@ __global__ void __launch_bounds__(256) k_attend_combine(AttendArgs a) {
 // do not change with the other rows in the batch.  Decode: groups of four
 // 32-key chunks per CTA, merged by k_attend_combine.  Prefill (many queries per
 // sequence): one CTA walks all chunks of its row.
-void attend_plan(int n_q, long long list_cap, int n_win, int &n_splits, int &cps) {
-  const long long chunks = (list_cap + n_win + kKC - 1) / kKC;
+void attend_plan(int n_q, long long list_cap, int n_win, bool tc, int &n_splits, int &cps) {
+  const int keys = tc ? 64 : kKC;               // keys per chunk of the kernel that runs
+  const long long chunks = (list_cap + n_win + keys - 1) / keys;
   if (n_q > 1) {
     cps = (int)chunks;
     n_splits = 1;
     return;
   }
-  cps = 4;
+  cps = tc ? 1 : 4;
   n_splits = (int)((chunks + cps - 1) / cps);
 }
 
@@ -251,6 +252,10 @@ cudaError_t launch_attend(const AttendArgs &a0, int rows, cudaStream_t st) {
   k_attend<<<grid, kAttThreads, smem, st>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || a.n_splits == 1) return e;
+  return launch_attend_combine(a, rows, st);
+}
+
+cudaError_t launch_attend_combine(const AttendArgs &a, int rows, cudaStream_t st) {
   k_attend_combine<<<dim3(a.heads, rows), 256, a.n_splits * sizeof(float), st>>>(a);
   return cudaGetLastError();
 }

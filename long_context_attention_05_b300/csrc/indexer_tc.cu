@@ -1,0 +1,369 @@
+// a2 — lightning-indexer scoring on the 5th-generation tensor cores (sm_103a).
+//
+// Sources: "DeepSeek V4: How They Crushed the Million-Token Memory Problem"
+// (sameershanbhag.com), "Two kinds of memory instead of one" — a low-precision
+// lightning indexer scores every compressed block with ReLU multi-head dot
+// products and keeps the top-k; "DeepSeek V4 infrastructure" (volanea.com),
+// "Compression only works if the attention path is engineered end to end" — a
+// selector whose scoring path burns memory bandwidth becomes the bottleneck.
+//
+// score_j = s_j * sum_h w_h * ReLU(q_h . code_j)  (s_j > 0 is the key's scale).
+//
+// Design.  The e4m3 keys stream from HBM once, by TMA, straight into the tensor
+// cores: D[entry, head] = sum_k code[entry, k] * q'[head, k] with
+// tcgen05.mma kind::f8f6f4, M = 128 entries (one TMEM lane each), N = heads,
+// K = 128 (four K=32 steps over one 128-byte swizzled row).  The bf16 query is
+// made an exact pair of e4m3 operands: per head a power of two S_h puts
+// max|q_h| below 2^8, hi = e4m3(q*S_h), lo = e4m3((q*S_h - hi) * 16); for every
+// component with |q*S_h| >= 2^-6 this is exact (8 significant bits = 4 + 4), so
+// the product q . code is the bf16 query's product up to fp32 accumulation.
+// Two accumulators (hi, lo) per tile, double-buffered in TMEM (4*heads columns).
+// The epilogue thread of TMEM lane l owns entry l of the tile:
+//   score = s_j * sum_h (w_h / S_h) * ReLU(D_hi[h] + D_lo[h] / 16).
+//
+// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer and TMEM
+// owner, warps 2..5 = epilogue (TMEM lane groups 2,3,0,1).  Pipelines: an
+// 8-stage shared-memory ring of key tiles (full/empty mbarriers) and two TMEM
+// accumulator buffers (tmem_full/tmem_empty).  Every wait is bounded; a
+// timeout sets the workspace status word and all roles stop issuing work.
+// grid = (CTAs per query row, query rows); each CTA scores a contiguous range of
+// 128-entry tiles of one row, so its query operand is built once.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "kernels.h"
+
+namespace csa {
+namespace {
+
+constexpr int kTileM = 128;
+constexpr int kDI = 128;
+constexpr int kStages = 8;
+constexpr int kStageBytes = kTileM * kDI;
+constexpr int kThreads = 192;
+constexpr long long kWaitLimit = 1LL << 24;
+
+struct TcArgs {
+  CacheView c;
+  int n_q, heads, q_dtype;
+  const uint8_t *q_idx;
+  const float *w;
+  float *scores;
+  long long stride;
+  int ctas_per_row;
+  int box_rows;       // rows per TMA box: 128 (contiguous) or the page size
+  int *status;        // workspace status word (may be null)
+};
+
+__device__ __forceinline__ uint32_t su32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(su32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase of `parity` to complete.  Gives up (returning
+// false) when another role has aborted or after kWaitLimit polls, in which case
+// it raises the abort flag and records CSA_ERR_TIMEOUT.
+__device__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int *status) {
+  for (long long i = 0; i < kWaitLimit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63) == 63 && *abort_flag) return false;
+  }
+  *abort_flag = 1;
+  if (status) atomicExch(status, CSA_ERR_TIMEOUT);
+  return false;
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+          su32(dst)),
+      "l"((uint64_t)map), "r"(su32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row
+// atoms 1024 bytes apart (sm_100 descriptor format, version 1).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+__device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+          d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+#define CSA_R8(i) "=r"(v[i]), "=r"(v[i + 1]), "=r"(v[i + 2]), "=r"(v[i + 3]), "=r"(v[i + 4]), "=r"(v[i + 5]), \
+                  "=r"(v[i + 6]), "=r"(v[i + 7])
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : CSA_R8(0), CSA_R8(8), CSA_R8(16), CSA_R8(24)
+      : "r"(taddr));
+}
+#undef CSA_R8
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant__ CUtensorMap kmap, TcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint8_t *stage = base;                                   // kStages x 16 KB key tiles
+  uint8_t *bhi = base + kStages * kStageBytes;             // [heads][128] e4m3, swizzled
+  uint8_t *blo = bhi + 128 * kDI;
+  float *wq = reinterpret_cast<float *>(blo + 128 * kDI);  // [heads] w_h / S_h
+  uint64_t *full = reinterpret_cast<uint64_t *>(wq + 128);
+  uint64_t *empty = full + kStages;
+  uint64_t *tfull = empty + kStages;
+  uint64_t *tempty = tfull + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const CacheView &c = a.c;
+  const int row = blockIdx.y;
+  const int b = row / a.n_q, iq = row % a.n_q;
+  const long long t = c.n_tokens[b] - a.n_q + iq;
+  const long long n_vis = min((t + 1) / c.m, c.cap);
+  const long long n_tiles = (n_vis + kTileM - 1) / kTileM;
+  const long long tile_lo = (long long)blockIdx.x * n_tiles / a.ctas_per_row;
+  const long long tile_hi = (long long)(blockIdx.x + 1) * n_tiles / a.ctas_per_row;
+  if (tile_lo >= tile_hi) return;   // uniform: nothing allocated yet
+  const int n_it = (int)(tile_hi - tile_lo);
+  const int H = a.heads;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    for (int s = 0; s < 2; ++s) { mbar_init(&tfull[s], 1); mbar_init(&tempty[s], 4); }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  const uint32_t ncols = H <= 32 ? 128u : (H <= 64 ? 256u : 512u);
+  uint32_t tmem = 0;
+  if (warp != 0) {
+    // ---- query operand (warps 1..5, while warp 0 already streams keys): per-head
+    //      power-of-two scale, exact e4m3 hi/lo split, written in the K-major
+    //      128-byte-swizzle layout the MMA reads
+    for (int h = warp - 1; h < H; h += kThreads / 32 - 1) {
+      float v[4];
+      const long long q0 = ((long long)row * H + h) * kDI + lane * 4;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[e] = load_tok(a.q_idx, a.q_dtype, q0 + e);
+      float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+      amax = warp_max(amax);
+      int ex = 0;
+      frexpf(amax, &ex);
+      const float S = amax > 0.f ? ldexpf(1.f, 8 - ex) : 1.f;   // amax * S < 2^8
+      uint32_t hw = 0, lw = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float x = v[e] * S;
+        const uint8_t hi = f32_to_e4m3_rn_sat(x);
+        const uint8_t lo = f32_to_e4m3_rn_sat((x - e4m3_to_f32(hi)) * 16.f);
+        hw |= (uint32_t)hi << (8 * e);
+        lw |= (uint32_t)lo << (8 * e);
+      }
+      const int k = lane * 4;   // 4 consecutive K bytes, inside one 16-byte chunk
+      const int off = h * kDI + ((((k >> 4) ^ (h & 7)) << 4) | (k & 15));
+      *reinterpret_cast<uint32_t *>(bhi + off) = hw;
+      *reinterpret_cast<uint32_t *>(blo + off) = lw;
+      if (lane == 0) wq[h] = a.w[(long long)row * H + h] / S;
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic-proxy writes -> tensor core reads
+    if (warp == 1) {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
+                   "r"(ncols)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    asm volatile("bar.sync 1, %0;" ::"n"(kThreads - 32) : "memory");   // warps 1..5 only
+    tc_fence_after();
+    tmem = *tmem_slot;
+  }
+
+  if (warp == 0) {
+    if (lane == 0) {   // ---- TMA producer
+      int issued = 0;
+      for (int it = 0; it < n_it; ++it) {
+        const int s = it % kStages;
+        const uint32_t ph = (uint32_t)(it / kStages) & 1u;
+        if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, a.status)) break;
+        mbar_expect_tx(&full[s], kStageBytes);
+        const long long tile = tile_lo + it;
+        if (c.page_size == 0) {
+          tma_load_2d(stage + s * kStageBytes, &kmap, &full[s], 0, (int)((long long)b * c.max_entries + tile * kTileM));
+        } else {
+          for (int r0 = 0; r0 < kTileM; r0 += a.box_rows) {
+            const long long j0 = tile * kTileM + r0;
+            long long lp = j0 / c.page_size;
+            if (lp >= c.max_pages) lp = 0;   // past the table: any valid page (never scored)
+            const long long pg = __ldg(c.page_table + (long long)b * c.max_pages + lp);
+            tma_load_2d(stage + s * kStageBytes + r0 * kDI, &kmap, &full[s], 0,
+                        (int)(pg * c.page_size + j0 % c.page_size));
+          }
+        }
+        ++issued;
+      }
+      if (*abort_flag) {   // let copies already issued land before shared memory goes away
+        for (int it = issued > kStages ? issued - kStages : 0; it < issued; ++it)
+          for (int i = 0; i < (1 << 20) && !mbar_try_wait(&full[it % kStages], (uint32_t)(it / kStages) & 1u); ++i) {
+          }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {   // ---- MMA issuer
+      const uint32_t idesc = (1u << 4) | ((uint32_t)(H >> 3) << 17) | ((uint32_t)(kTileM >> 4) << 24);
+      const uint32_t bh = su32(bhi), bl = su32(blo);
+      for (int it = 0; it < n_it; ++it) {
+        const int s = it % kStages;
+        const uint32_t ph = (uint32_t)(it / kStages) & 1u;
+        const int acc = it & 1;
+        const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+        if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, a.status)) break;
+        if (!mbar_wait(&full[s], ph, abort_flag, a.status)) break;
+        tc_fence_after();
+        const uint32_t as = su32(stage + s * kStageBytes);
+        const uint32_t d_hi = tmem + (uint32_t)(acc * 2 * H), d_lo = d_hi + (uint32_t)H;
+#pragma unroll
+        for (int kk = 0; kk < kDI / 32; ++kk) {
+          const uint64_t ad = sw128_desc(as + kk * 32);
+          umma_f8(d_hi, ad, sw128_desc(bh + kk * 32), idesc, kk > 0);
+          umma_f8(d_lo, ad, sw128_desc(bl + kk * 32), idesc, kk > 0);
+        }
+        umma_commit(&empty[s]);
+        umma_commit(&tfull[acc]);
+      }
+    }
+  } else {   // ---- epilogue: TMEM lane group g = warp % 4 owns entries 32g .. 32g+31 of a tile
+    const int g = warp & 3;
+    // key scales are read four tiles ahead so their memory latency overlaps the
+    // tiles in between instead of stalling each tile's epilogue
+    auto scale_of = [&](int it2) -> float {
+      const long long j2 = (tile_lo + it2) * kTileM + g * 32 + lane;
+      return (it2 < n_it && j2 < n_vis) ? __ldg(c.idx_scale + entry_row(c, b, j2)) : 0.f;
+    };
+    float sc0 = scale_of(0), sc1 = scale_of(1), sc2 = scale_of(2), sc3 = scale_of(3);
+    for (int it = 0; it < n_it; ++it) {
+      const int acc = it & 1;
+      const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+      const bool ok = mbar_wait(&tfull[acc], aph, abort_flag, a.status);
+      if (!__all_sync(0xffffffffu, ok)) break;   // warp-uniform: the TMEM loads below are .sync.aligned
+      tc_fence_after();
+      const uint32_t taddr = tmem + ((uint32_t)(g * 32) << 16) + (uint32_t)(acc * 2 * H);
+      float sum = 0.f;
+      for (int c0 = 0; c0 < H; c0 += 32) {
+        uint32_t hv[32], lv[32];
+        tmem_ld32(taddr + c0, hv);
+        tmem_ld32(taddr + H + c0, lv);
+        tmem_wait_ld();
+#pragma unroll
+        for (int h = 0; h < 32; ++h)
+          sum = fmaf(wq[c0 + h], fmaxf(fmaf(__uint_as_float(lv[h]), 0.0625f, __uint_as_float(hv[h])), 0.f), sum);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      const long long j = (tile_lo + it) * kTileM + g * 32 + lane;
+      if (j < n_vis) a.scores[(long long)row * a.stride + j] = sum * sc0;
+      sc0 = sc1; sc1 = sc2; sc2 = sc3; sc3 = scale_of(it + 4);
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+}  // namespace
+
+bool index_tc_supported(const CacheView &c, int heads_idx) {
+  if (c.kv_dtype != CSA_E4M3 || c.d_idx != kDI) return false;
+  if (heads_idx != 32 && heads_idx != 64 && heads_idx != 128) return false;
+  if (c.page_size != 0) {
+    const int p = c.page_size;
+    if (p < 8 || (p & (p - 1))) return false;
+  }
+  return true;
+}
+
+size_t index_tc_smem_bytes() {
+  return 1024 + (size_t)kStages * kStageBytes + 2 * 128 * kDI + 128 * sizeof(float) + (2 * kStages + 4) * 8 + 16;
+}
+
+cudaError_t launch_index_tc(const CacheView &c, int batch, int n_q, const void *q_idx, int q_dtype, const float *w,
+                            int heads_idx, float *scores, long long stride, int num_sms, int *status,
+                            cudaStream_t st) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  CUtensorMap map;
+  const int box_rows = c.page_size == 0 ? kTileM : (c.page_size < kTileM ? c.page_size : kTileM);
+  // contiguous: the real row extent, so a tail tile past it reads zeros; paged:
+  // rows are reached only through valid page ids, the extent is not known here
+  const cuuint64_t rows = c.page_size == 0 ? (cuuint64_t)batch * (cuuint64_t)c.max_entries : (cuuint64_t)0x7fffffff;
+  cuuint64_t gdim[2] = {(cuuint64_t)kDI, rows};
+  cuuint64_t gstride[1] = {(cuuint64_t)kDI};
+  cuuint32_t box[2] = {(cuuint32_t)kDI, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, (void *)c.idx_key, gdim, gstride, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  TcArgs a;
+  a.c = c; a.n_q = n_q; a.heads = heads_idx; a.q_dtype = q_dtype;
+  a.q_idx = (const uint8_t *)q_idx; a.w = w; a.scores = scores; a.stride = stride;
+  a.box_rows = box_rows; a.status = status;
+  const int rows_q = batch * n_q;
+  const long long max_tiles = (c.cap + kTileM - 1) / kTileM;
+  long long cpr = (num_sms + rows_q - 1) / rows_q;
+  if (cpr > max_tiles) cpr = max_tiles;
+  if (cpr < 1) cpr = 1;
+  a.ctas_per_row = (int)cpr;
+  const size_t smem = index_tc_smem_bytes();
+  cudaError_t e = cudaFuncSetAttribute(k_index_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  k_index_tc<<<dim3((unsigned)cpr, rows_q), kThreads, smem, st>>>(map, a);
+  return cudaGetLastError();
+}
+
+}  // namespace csa

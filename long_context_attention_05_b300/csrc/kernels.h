@@ -12,8 +12,14 @@ cudaError_t launch_index_generic(const CacheView &c, int batch, int n_q, const v
                                  const float *w, int heads_idx, float *scores, long long stride,
                                  long long n_cap, cudaStream_t st);
 
+bool index_tc_supported(const CacheView &c, int heads_idx);
+size_t index_tc_smem_bytes();
+cudaError_t launch_index_tc(const CacheView &c, int batch, int n_q, const void *q_idx, int q_dtype, const float *w,
+                            int heads_idx, float *scores, long long stride, int num_sms, int *status,
+                            cudaStream_t st);
+
 cudaError_t launch_topk(const CacheView &c, int batch, int n_q, const float *scores, long long stride, int k,
-                        int32_t *out_idx, int32_t *out_count, cudaStream_t st);
+                        int32_t *out_idx, int32_t *out_count, int num_sms, cudaStream_t st);
 
 constexpr int kHG = 16;
 constexpr int kKC = 32;
@@ -31,8 +37,12 @@ struct AttendArgs {
   float *out_lse;
   float scale;          // 1/sqrt(d)
 };
-void attend_plan(int n_q, long long list_cap, int n_win, int &n_splits, int &cps);
+void attend_plan(int n_q, long long list_cap, int n_win, bool tc, int &n_splits, int &cps);
+bool attend_tc_supported(const CacheView &c, int heads, int q_dtype);
+size_t attend_tc_smem_bytes(int d);
+cudaError_t launch_attend_tc(const AttendArgs &a, int rows, cudaStream_t st);
 size_t attend_smem_bytes(int d);
 cudaError_t launch_attend(const AttendArgs &a, int rows, cudaStream_t st);
+cudaError_t launch_attend_combine(const AttendArgs &a, int rows, cudaStream_t st);
 
 }  // namespace csa

@@ -1,0 +1,84 @@
+"""Reproducibility properties of the CUDA path (the write-ups stress bitwise
+reproducible, batch-invariant kernels): identical bits on a rerun, for a
+sequence alone versus inside a batch, and for a paged cache versus the same
+entries stored contiguously."""
+import numpy as np
+import pytest
+import torch
+
+import harness as H
+from long_context_attention_05_b300 import synthetic as S
+
+pytestmark = pytest.mark.gpu
+
+
+def _same(a, b, keys=("idx", "cnt", "o", "lse")):
+    for k in keys:
+        if k in a:
+            assert np.array_equal(a[k], b[k], equal_nan=True), k
+
+
+def _setup(w):
+    inp = S.step_inputs(w)
+    arrs = S.seeded_cache(w, inp.get("q_idx"), inp.get("w_idx"))
+    return arrs, inp
+
+
+@pytest.mark.parametrize("kind", ["csa", "hca"])
+def test_rerun_is_bitwise_identical(kind):
+    w = S.config2(ctx=(65536, 40000, 8192, 100000)) if kind == "csa" else S.config1(batch=3, ctx=(131072, 65536, 1024))
+    arrs, inp = _setup(w)
+    a = H.gpu_seeded_step(w, arrs, inp)
+    b = H.gpu_seeded_step(w, arrs, inp)
+    _same(a, b, ("idx", "cnt", "o", "lse", "scores"))
+
+
+def _slice_batch(w, arrs, inp, b):
+    """Sequence b of a contiguous seeded cache as a batch of one (same bytes)."""
+    import dataclasses
+    extra = w.max_entries - (w.ctx[b] // w.m + w.n_new // w.m + 1)   # keep the batch's entry capacity
+    w1 = dataclasses.replace(w, batch=1, ctx=(w.ctx[b],), extra_entries=extra)
+    rows = slice(b * w.max_entries, (b + 1) * w.max_entries)
+    a1 = {k: (v[rows] if k in ("kv_nope", "kv_scale", "kv_rope", "idx_key", "idx_scale") else v) for k, v in arrs.items()}
+    # the single sequence keeps the batch's entry capacity
+    a1["win"] = arrs["win"][b:b + 1]
+    a1["pool_state"] = arrs["pool_state"][b:b + 1]
+    a1["n_tokens"] = arrs["n_tokens"][b:b + 1]
+    i1 = {k: (v[b:b + 1] if v.ndim >= 2 and v.shape[0] == w.batch else v) for k, v in inp.items()}
+    return w1, a1, i1
+
+
+def test_batch_invariance():
+    w = S.config2(ctx=(65536, 40000, 8192, 100000), extra_entries=64)
+    arrs, inp = _setup(w)
+    full = H.gpu_seeded_step(w, arrs, inp)
+    for b in (0, 2, 3):
+        w1, a1, i1 = _slice_batch(w, arrs, inp, b)
+        assert w1.max_entries == w.max_entries
+        one = H.gpu_seeded_step(w1, a1, i1)
+        for k in ("idx", "cnt", "o", "lse"):
+            assert np.array_equal(one[k][0], full[k][b]), (b, k)
+
+
+def test_paged_equals_contiguous():
+    import dataclasses
+    w = S.config2(batch=3, ctx=(65536, 40000, 8192), extra_entries=64)
+    arrs, inp = _setup(w)
+    cont = H.gpu_seeded_step(w, arrs, inp)
+    wp = dataclasses.replace(w, page_size=64, spare_pages=5)
+    n_pages = w.batch * wp.max_pages + wp.spare_pages
+    perm = np.random.default_rng(5).permutation(n_pages).astype(np.int32)
+    pt = perm[: w.batch * wp.max_pages].reshape(w.batch, wp.max_pages)
+    ap = dict(arrs)
+    for name in ("kv_nope", "kv_scale", "kv_rope", "idx_key", "idx_scale"):
+        src = arrs[name]
+        dst = np.zeros((n_pages * 64,) + src.shape[1:], dtype=src.dtype)
+        for b in range(w.batch):
+            n = w.max_entries
+            j = np.arange(wp.max_pages * 64)
+            j = j[j < n]
+            dst[pt[b, j // 64].astype(np.int64) * 64 + j % 64] = src[b * w.max_entries + j]
+        ap[name] = dst
+    ap["page_table"] = pt
+    paged = H.gpu_seeded_step(wp, ap, inp)
+    _same(cont, paged)

@@ -156,3 +156,13 @@ def test_c4_stack_small_paged():
         arrs, inp = _seeded(w)
         res = H.gpu_seeded_step(w, arrs, inp)
         _check_step(w, arrs, inp, res, H.TOL_LOW, what=w.name)
+
+
+@pytest.mark.parametrize("heads_idx", [32, 128, 48])
+def test_indexer_head_counts(heads_idx):
+    """32/64/128 indexer heads take the tensor-core kernel; other counts the
+    CUDA-core kernel.  Both against the oracle."""
+    w = S.config2(ctx=(8192, 20000, 4096, 131072), heads_idx=heads_idx, k=512)
+    arrs, inp = _seeded(w)
+    res = H.gpu_seeded_step(w, arrs, inp)
+    _check_step(w, arrs, inp, res, H.TOL_LOW, what=f"h_idx={heads_idx}")
