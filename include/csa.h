@@ -206,6 +206,33 @@ CSA_API csa_status hca_attend(const csa_cache *cache, int batch, int n_q, const 
                       size_t ws_bytes, csa_stream_t stream);
 
 /*
+ * csa_index_topk without a workspace argument, for callers that cannot allocate
+ * device memory.  (The paper has no counterpart: this is a deployment variant.)
+ * Some hosts hand a library only its input and output buffers: an engine that
+ * reserved all device memory for its own pool up front, a plugin interface that
+ * exposes no allocator, or a latency-critical loop where cudaMalloc/cudaFree
+ * (which can synchronise the device) are not allowed.  This entry point keeps
+ * its scratch -- the indexer scores of every query row plus the status word --
+ * in one statically sized device array inside the library, so the call itself
+ * allocates nothing.
+ *   - Capacity: CSA_STATIC_SCRATCH_BYTES.  The call needs 256 bytes plus
+ *     batch * n_q * entry capacity * 4 bytes (rounded up to 256); a larger
+ *     request returns CSA_ERR_WORKSPACE and launches nothing.
+ *   - The array exists once per device for the life of the process, on every
+ *     device that loads the library.  The first call on a device looks up the
+ *     array's device address (cudaGetSymbolAddress, with that device current);
+ *     make that first call before any stream capture.
+ *   - All calls share the one array and its contents outlive a call: calls that
+ *     may overlap on the GPU (different streams, or devices sharing a context)
+ *     race on it.  Serialise them.  The status word is cleared on each call.
+ *   - Results are those of csa_index_topk on the same inputs.
+ */
+#define CSA_STATIC_SCRATCH_BYTES ((size_t)8 << 20)
+CSA_API csa_status csa_index_topk_static(const csa_cache *cache, int batch, int n_q, const void *q_idx,
+                                         int q_dtype, const float *w, int heads_idx, int k, int32_t *out_idx,
+                                         int32_t *out_count, csa_stream_t stream);
+
+/*
  * Reads (synchronously, on `stream`) and clears the device status word at the
  * start of a workspace: 0 = fine, otherwise a CSA_ERR_* code set by a kernel
  * whose bounded wait gave up.  Returns CSA_OK or CSA_ERR_CUDA.

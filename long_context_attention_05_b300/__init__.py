@@ -23,7 +23,8 @@ CSA_OK = 0
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "WORKSPACE", 4: "CUDA", 5: "TIMEOUT"}
 
 EXPORTS = ("csa_version", "csa_last_error", "csa_workspace_size", "csa_compress", "csa_index_scores", "csa_topk",
-           "csa_index_topk", "csa_sparse_attend", "hca_attend", "csa_device_status")
+           "csa_index_topk", "csa_sparse_attend", "hca_attend", "csa_device_status", "csa_index_topk_static")
+STATIC_SCRATCH_BYTES = 8 << 20
 
 
 class CsaCacheStruct(ctypes.Structure):
@@ -59,6 +60,7 @@ def lib() -> ctypes.CDLL:
         L.csa_index_scores.argtypes = [C, I, I, P, I, P, I, P, I64, P, SZ, P]
         L.csa_topk.argtypes = [C, I, I, P, I64, I, P, P, P, SZ, P]
         L.csa_index_topk.argtypes = [C, I, I, P, I, P, I, I, P, P, P, SZ, P]
+        L.csa_index_topk_static.argtypes = [C, I, I, P, I, P, I, I, P, P, P]
         L.csa_sparse_attend.argtypes = [C, I, I, P, I, I, P, P, I, P, I, P, P, SZ, P]
         L.hca_attend.argtypes = [C, I, I, P, I, I, P, P, I, P, P, SZ, P]
         L.csa_device_status.argtypes = [P, ctypes.POINTER(I), P]
@@ -215,6 +217,18 @@ def csa_index_topk(cache: Cache, q_idx, w, k, out_idx, out_count, ws, stream=Non
     st = lib().csa_index_topk(cache.ref, B, n_q, _ptr(q_idx), _dtype_code(q_idx), _ptr(w), H_I, k, _ptr(out_idx),
                               _ptr(out_count), p, n, _stream(stream))
     _check(st, "csa_index_topk")
+
+
+def csa_index_topk_static(cache: Cache, q_idx, w, k, out_idx, out_count, stream=None):
+    """csa_index_topk with the library's own static device scratch instead of a
+    caller workspace (for callers that cannot allocate; calls must not overlap)."""
+    B, n_q, H_I = q_idx.shape[0], q_idx.shape[1], q_idx.shape[2]
+    _need(w, torch.float32, "w")
+    _need(out_idx, torch.int32, "out_idx")
+    _need(out_count, torch.int32, "out_count")
+    st = lib().csa_index_topk_static(cache.ref, B, n_q, _ptr(q_idx), _dtype_code(q_idx), _ptr(w), H_I, k,
+                                     _ptr(out_idx), _ptr(out_count), _stream(stream))
+    _check(st, "csa_index_topk_static")
 
 
 def csa_sparse_attend(cache: Cache, q, sink, idx, out, out_lse=None, ws=None, stream=None):

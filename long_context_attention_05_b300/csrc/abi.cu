@@ -6,6 +6,7 @@
 #include <cstdio>
 #include <algorithm>
 #include <cstring>
+#include <mutex>
 #include <string>
 
 #include "kernels.h"
@@ -211,6 +212,39 @@ cudaError_t launch_indexer(const csa_cache *c, int batch, int n_q, const void *q
 
 }  // namespace
 
+// Scratch of csa_index_topk_static: one array per device, reused by every call.
+static __device__ __align__(256) unsigned char g_static_scratch[CSA_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+// Device address of g_static_scratch on the current device, looked up once per
+// device (cudaGetSymbolAddress with that device current).  Host code only sees
+// a host-side stand-in for the array; kernels must get this address instead.
+void *static_scratch(csa_status &st) {
+  static std::mutex mu;
+  static void *addr[256] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 256) {
+    st = cuda_status(e == cudaSuccess ? cudaErrorInvalidDevice : e, "current device");
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess || !p) {
+      st = cuda_status(e == cudaSuccess ? cudaErrorInvalidSymbol : e, "static scratch address");
+      return nullptr;
+    }
+    addr[dev] = p;
+  }
+  st = CSA_OK;
+  return addr[dev];
+}
+
+}  // namespace
+
 extern "C" {
 
 int csa_version(void) { return 100; }
@@ -284,6 +318,31 @@ csa_status csa_index_topk(const csa_cache *c, int batch, int n_q, const void *q_
   cudaError_t e = launch_indexer(c, batch, n_q, q_idx, q_dtype, w, heads_idx, scores, cap, ws, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_status(e, "indexer launch");
   return cuda_status(csa::launch_topk(view(c), batch, n_q, scores, cap, k, out_idx, out_count, num_sms(), (cudaStream_t)stream),
+                     "top-k launch");
+}
+
+csa_status csa_index_topk_static(const csa_cache *c, int batch, int n_q, const void *q_idx, int q_dtype,
+                                 const float *w, int heads_idx, int k, int32_t *out_idx, int32_t *out_count,
+                                 csa_stream_t stream) {
+  csa_status s = check_index_args(c, batch, n_q, q_idx, q_dtype, w, heads_idx);
+  if (s) return s;
+  if (k < 1) return fail(CSA_ERR_INVALID_ARG, "k must be >= 1");
+  if (!out_idx || !out_count) return fail(CSA_ERR_INVALID_ARG, "NULL output pointer");
+  const size_t need = kHeader + scores_bytes(c, batch, n_q);
+  if (need > CSA_STATIC_SCRATCH_BYTES)
+    return fail(CSA_ERR_WORKSPACE,
+                "needs %zu bytes of scratch (%d rows x %lld entries); the static scratch holds %zu bytes",
+                need, batch * n_q, entry_cap(c), (size_t)CSA_STATIC_SCRATCH_BYTES);
+  void *ws = static_scratch(s);
+  if (!ws) return s;
+  cudaError_t e = cudaMemsetAsync(ws, 0, kHeader, (cudaStream_t)stream);   // status word starts at zero
+  if (e != cudaSuccess) return cuda_status(e, "static scratch clear");
+  float *scores = (float *)((char *)ws + kHeader);
+  const long long cap = entry_cap(c);
+  e = launch_indexer(c, batch, n_q, q_idx, q_dtype, w, heads_idx, scores, cap, ws, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_status(e, "indexer launch");
+  return cuda_status(csa::launch_topk(view(c), batch, n_q, scores, cap, k, out_idx, out_count, num_sms(),
+                                      (cudaStream_t)stream),
                      "top-k launch");
 }
 
