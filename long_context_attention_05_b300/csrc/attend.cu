@@ -187,46 +187,69 @@ __global__ void __launch_bounds__(kAttThreads) k_attend(AttendArgs a) {
 }
 
 // Merge of split partials: M = max(sink, m_s), L = exp(sink-M) + sum_s l_s exp(m_s-M),
-// out = sum_s o_s exp(m_s-M) / L, lse = M + log L.  Fixed split order.
+// out = sum_s o_s exp(m_s-M) / L, lse = M + log L.  Fixed split order (each
+// element's sum runs over s = 0, 1, ... in the same order on every call).
+// The split weights are computed in parallel; each thread keeps 8 partial loads
+// in flight instead of walking the splits one memory round trip at a time.
 __global__ void __launch_bounds__(256) k_attend_combine(AttendArgs a) {
   extern __shared__ float wts[];   // [n_splits]
+  __shared__ float red[8];
   __shared__ float sh_M, sh_L;
   const int h = blockIdx.x, row = blockIdx.y;
-  const int d = a.c.d;
+  const int d = a.c.d, S = a.n_splits;
   const float z = __ldg(a.sink + h);
-  const long long base = (long long)row * a.n_splits * a.heads + h;
-  if (threadIdx.x == 0) {
-    float M = z;
-    for (int s = 0; s < a.n_splits; ++s) M = fmaxf(M, a.part_ml[(base + (long long)s * a.heads) * 2]);
-    float L = expf(z - M);
-    for (int s = 0; s < a.n_splits; ++s) {
-      const float ms = a.part_ml[(base + (long long)s * a.heads) * 2];
-      const float w = ms > -INFINITY ? expf(ms - M) : 0.f;
-      wts[s] = w;
-      L += w * a.part_ml[(base + (long long)s * a.heads) * 2 + 1];
-    }
+  const long long base = (long long)row * S * a.heads + h;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // M over splits and the sink
+  float m = z;
+  for (int s = tid; s < S; s += blockDim.x) m = fmaxf(m, a.part_ml[(base + (long long)s * a.heads) * 2]);
+  m = warp_max(m);
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+  if (tid == 0) {
+    float M = red[0];
+    for (int i = 1; i < (int)(blockDim.x >> 5); ++i) M = fmaxf(M, red[i]);
     sh_M = M;
+  }
+  __syncthreads();
+  const float M = sh_M;
+  for (int s = tid; s < S; s += blockDim.x) {
+    const float ms = a.part_ml[(base + (long long)s * a.heads) * 2];
+    wts[s] = ms > -INFINITY ? expf(ms - M) : 0.f;
+  }
+  __syncthreads();
+  if (tid == 0) {   // fixed order over splits
+    float L = expf(z - M);
+    for (int s = 0; s < S; ++s) L += wts[s] * a.part_ml[(base + (long long)s * a.heads) * 2 + 1];
     sh_L = L;
   }
   __syncthreads();
   const float invL = 1.f / sh_L;
   const long long ob = ((long long)row * a.heads + h) * d;
-  for (int e = threadIdx.x; e < d; e += blockDim.x) {
+  for (int e = tid; e < d; e += blockDim.x) {
     float o = 0.f;
-    for (int s = 0; s < a.n_splits; ++s)
-      if (wts[s] != 0.f) o = fmaf(wts[s], a.part_o[(base + (long long)s * a.heads) * d + e], o);
+    for (int s0 = 0; s0 < S; s0 += 8) {
+      float v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        v[q] = (s0 + q < S && wts[s0 + q] != 0.f) ? a.part_o[(base + (long long)(s0 + q) * a.heads) * d + e] : 0.f;
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (s0 + q < S) o = fmaf(wts[s0 + q], v[q], o);
+    }
     o *= invL;
     if (a.out_dtype == CSA_F32) reinterpret_cast<float *>(a.out)[ob + e] = o;
     else reinterpret_cast<uint16_t *>(a.out)[ob + e] = f32_to_bf16_rn(o);
   }
-  if (threadIdx.x == 0 && a.out_lse) a.out_lse[(long long)row * a.heads + h] = sh_M + logf(sh_L);
+  if (tid == 0 && a.out_lse) a.out_lse[(long long)row * a.heads + h] = sh_M + logf(sh_L);
 }
 
 // Split plan shared by the launcher and the workspace sizing.  It depends only
 // on the key-list capacity and on whether the call is a decode (one query per
 // sequence), never on the batch, so a row's reduction order -- and its bits --
-// do not change with the other rows in the batch.  Decode: groups of four
-// 32-key chunks per CTA, merged by k_attend_combine.  Prefill (many queries per
+// do not change with the other rows in the batch.  Decode: one 64-key chunk
+// per CTA (tensor-core kernel) or four 32-key chunks (CUDA-core kernel), merged
+// by k_attend_combine.  Prefill (many queries per
 // sequence): one CTA walks all chunks of its row.
 void attend_plan(int n_q, long long list_cap, int n_win, bool tc, int &n_splits, int &cps) {
   const int keys = tc ? 64 : kKC;               // keys per chunk of the kernel that runs

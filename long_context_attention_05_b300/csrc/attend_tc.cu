@@ -77,6 +77,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttendArgs a) {
   float *l_run = m_run + kHeadsMax;
   float *corr = l_run + kHeadsMax;
   long long *ksrc = reinterpret_cast<long long *>(corr + kHeadsMax);    // [64]
+  float2 *qcs = reinterpret_cast<float2 *>(ksrc + kKeys);               // [32] (cos, sin) at t
 
   const CacheView &c = a.c;
   const int row = blockIdx.y;
@@ -90,25 +91,76 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttendArgs a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = warp & 3, qq = warp >> 2;
 
-  // ---- query: warp w converts heads w, w+16, ...; lane holds D/32 consecutive dims
+  // key source of slot tid of a chunk: entry row (>= 0), -2 - position (window
+  // token) or -1 (no key); sigma as described above
+  auto key_src = [&](long long u0) {
+    const long long u = u0 + tid;
+    long long src = -1;
+    if (u < n_list) {
+      const long long j = a.idx ? (long long)__ldg(a.idx + (long long)row * a.k + u) : u;
+      if (j >= 0 && j < n_vis) src = entry_row(c, b, j);
+    } else if (u < U) {
+      const long long tau = t - c.n_win + 1 + (u - n_list);
+      if (tau >= 0) src = -2 - tau;
+    }
+    return src;
+  };
+  const long long ch0 = (long long)split * a.chunks_per_split;
+  // the first chunk's key lookups go out before the query work, to overlap
+  long long src_next = -1;
+  float sig_next = 0.f;
+  if (tid < kKeys && ch0 * kKeys < U) {
+    src_next = key_src(ch0 * kKeys);
+    sig_next = src_next >= 0 ? 256.f * __ldg(c.kv_scale + src_next) : (src_next <= -2 ? 1.f : 0.f);
+  }
+
+  // ---- query: one (cos, sin) per rotary pair at t, shared by all heads
+  if (tid < 32) {
+    float cs, sn;
+    rope_cos_sin(t, a.rope.step[tid], cs, sn);
+    qcs[tid] = make_float2(cs, sn);
+  }
+  __syncthreads();
+  // warp w converts heads w, w+16, ...; lane holds D/32 consecutive dims
   {
     constexpr int PER = D / 32;
-    for (int h = warp; h < kHeadsMax; h += kThreads / 32) {
+#pragma unroll
+    for (int hh = 0; hh < kHeadsMax / (kThreads / 32); ++hh) {
+      const int h = warp + hh * (kThreads / 32);
       float v[PER];
       if (h < H) {
         const long long q0 = ((long long)row * H + h) * D + lane * PER;
+        if (a.q_dtype == CSA_BF16 && PER % 8 == 0) {   // 16-byte loads
+          const uint4 *src = reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(a.q) + q0);
 #pragma unroll
-        for (int e = 0; e < PER; ++e) v[e] = load_tok(a.q, a.q_dtype, q0 + e);
+          for (int u = 0; u < PER / 8; ++u) {
+            const uint4 x = __ldg(src + u);
+            const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              v[u * 8 + 2 * e] = bf16_bits_to_f32((uint16_t)(w4[e] & 0xFFFF));
+              v[u * 8 + 2 * e + 1] = bf16_bits_to_f32((uint16_t)(w4[e] >> 16));
+            }
+          }
+        } else if (a.q_dtype == CSA_BF16 && PER == 4) {   // d = 128: one 8-byte load
+          const uint2 x = __ldg(reinterpret_cast<const uint2 *>(reinterpret_cast<const uint16_t *>(a.q) + q0));
+          v[0] = bf16_bits_to_f32((uint16_t)(x.x & 0xFFFF));
+          v[1] = bf16_bits_to_f32((uint16_t)(x.x >> 16));
+          v[2] = bf16_bits_to_f32((uint16_t)(x.y & 0xFFFF));
+          v[3] = bf16_bits_to_f32((uint16_t)(x.y >> 16));
+        } else {
+#pragma unroll
+          for (int e = 0; e < PER; ++e) v[e] = load_tok(a.q, a.q_dtype, q0 + e);
+        }
         // rotary turn of the pairs this lane holds (last 64 dims)
 #pragma unroll
         for (int e = 0; e < PER; e += 2) {
           const int dim = lane * PER + e;
           if (dim >= DN) {
-            float cs, sn;
-            rope_cos_sin(t, a.rope.step[(dim - DN) >> 1], cs, sn);
+            const float2 cs = qcs[(dim - DN) >> 1];
             const float x0 = v[e], x1 = v[e + 1];
-            v[e] = fmaf(x0, cs, -x1 * sn);
-            v[e + 1] = fmaf(x0, sn, x1 * cs);
+            v[e] = fmaf(x0, cs.x, -x1 * cs.y);
+            v[e + 1] = fmaf(x0, cs.y, x1 * cs.x);
           }
         }
       } else {
@@ -139,42 +191,59 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttendArgs a) {
 #pragma unroll
     for (int r = 0; r < 4; ++r) acc[n][r] = 0.f;
 
-  const long long ch0 = (long long)split * a.chunks_per_split;
   for (long long chunk = ch0; chunk < ch0 + a.chunks_per_split; ++chunk) {
     const long long u0 = chunk * kKeys;
     if (u0 >= U) break;
     __syncthreads();   // previous chunk's value phase is done with Ks / P
     if (tid < kKeys) {
-      const long long u = u0 + tid;
-      long long src = -1;
-      float sg = 0.f;
-      if (u < n_list) {
-        const long long j = a.idx ? (long long)a.idx[(long long)row * a.k + u] : u;
-        if (j >= 0 && j < n_vis) {
-          src = entry_row(c, b, j);
-          sg = 256.f * __ldg(c.kv_scale + src);
-        }
-      } else if (u < U) {
-        const long long tau = t - c.n_win + 1 + (u - n_list);
-        if (tau >= 0) { src = -2 - tau; sg = 1.f; }
+      ksrc[tid] = src_next;
+      sig[tid] = sig_next;
+      // look up the next chunk's keys now; used one chunk later
+      const long long u1 = u0 + kKeys;
+      src_next = -1;
+      sig_next = 0.f;
+      if (chunk + 1 < ch0 + a.chunks_per_split && u1 < U) {
+        src_next = key_src(u1);
+        sig_next = src_next >= 0 ? 256.f * __ldg(c.kv_scale + src_next) : (src_next <= -2 ? 1.f : 0.f);
       }
-      ksrc[tid] = src;
-      sig[tid] = sg;
     }
     __syncthreads();
-    // ---- gather the key tile as f16: 16-byte pieces
+    // ---- gather the key tile as f16, in 16-byte pieces: every thread first issues
+    //      all of its loads, then converts and stores (one memory latency per chunk)
     {
       constexpr int NOPE16 = DN / 16;   // 16-byte e4m3 pieces per entry
       constexpr int ROPE16 = 64 / 8;    // 16-byte bf16 pieces of the rotary dims
       constexpr int RAW16 = D / 8;      // 16-byte bf16 pieces of a raw window token
       constexpr int PIECES = NOPE16 > RAW16 - ROPE16 ? NOPE16 + ROPE16 : RAW16;
-      for (int x = tid; x < kKeys * PIECES; x += kThreads) {
+      constexpr int PER_T = (kKeys * PIECES + kThreads - 1) / kThreads;
+      uint4 buf[PER_T];
+#pragma unroll
+      for (int r = 0; r < PER_T; ++r) {
+        const int x = tid + r * kThreads;
+        buf[r] = make_uint4(0, 0, 0, 0);
+        if (x < kKeys * PIECES) {
+          const int kk = x / PIECES, p = x % PIECES;
+          const long long src = ksrc[kk];
+          if (src >= 0) {
+            if (p < NOPE16) buf[r] = __ldg(reinterpret_cast<const uint4 *>(c.kv_nope + src * DN) + p);
+            else if (p < NOPE16 + ROPE16)
+              buf[r] = __ldg(reinterpret_cast<const uint4 *>(c.kv_rope + src * 64 * 2) + (p - NOPE16));
+          } else if (src <= -2 && p < RAW16) {
+            const long long tau = -2 - src;
+            buf[r] = __ldg(reinterpret_cast<const uint4 *>(c.win + ((long long)b * c.win_cap + tau % c.win_cap) * D * 2) + p);
+          }
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < PER_T; ++r) {
+        const int x = tid + r * kThreads;
+        if (x >= kKeys * PIECES) continue;
         const int kk = x / PIECES, p = x % PIECES;
         const long long src = ksrc[kk];
         __half *dst = Ks + kk * LDQ;
+        const uint4 u = buf[r];
         if (src >= 0) {
           if (p < NOPE16) {
-            const uint4 u = __ldg(reinterpret_cast<const uint4 *>(c.kv_nope + src * DN) + p);
             uint4 o0, o1;
             o0.x = e4m3x2_to_f16x2_scaled(u.x); o0.y = e4m3x2_to_f16x2_scaled(u.x >> 16);
             o0.z = e4m3x2_to_f16x2_scaled(u.y); o0.w = e4m3x2_to_f16x2_scaled(u.y >> 16);
@@ -183,21 +252,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttendArgs a) {
             *reinterpret_cast<uint4 *>(dst + p * 16) = o0;
             *reinterpret_cast<uint4 *>(dst + p * 16 + 8) = o1;
           } else if (p < NOPE16 + ROPE16) {
-            const int r = p - NOPE16;
-            const uint4 u = __ldg(reinterpret_cast<const uint4 *>(c.kv_rope + src * 64 * 2) + r);
             const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
             uint4 o;
             uint32_t *op = &o.x;
 #pragma unroll
             for (int e = 0; e < 4; ++e)
               op[e] = pack_h2(bf16_bits_to_f32((uint16_t)(w4[e] & 0xFFFF)), bf16_bits_to_f32((uint16_t)(w4[e] >> 16)));
-            *reinterpret_cast<uint4 *>(dst + DN + r * 8) = o;
+            *reinterpret_cast<uint4 *>(dst + DN + (p - NOPE16) * 8) = o;
           }
         } else if (src <= -2) {
           if (p < RAW16) {
             const long long tau = -2 - src;
-            const uint4 u = __ldg(reinterpret_cast<const uint4 *>(
-                                      c.win + ((long long)b * c.win_cap + tau % c.win_cap) * D * 2) + p);
             const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
             float f[8];
 #pragma unroll
@@ -374,7 +439,7 @@ bool attend_tc_supported(const CacheView &c, int heads, int q_dtype) {
 
 size_t attend_tc_smem_bytes(int d) {
   return (size_t)(2 * kHeadsMax * (d + kPadH)) * 2 + (size_t)kHeadsMax * (kKeys + 4) * 4 +
-         (size_t)2 * kHeadsMax * (kKeys + kPadH) * 2 + (size_t)(kKeys + 4 * kHeadsMax) * 4 + kKeys * 8;
+         (size_t)2 * kHeadsMax * (kKeys + kPadH) * 2 + (size_t)(kKeys + 4 * kHeadsMax) * 4 + kKeys * 8 + 32 * 8;
 }
 
 cudaError_t launch_attend_tc(const AttendArgs &a, int rows, cudaStream_t st) {

@@ -21,10 +21,11 @@
 // The epilogue thread of TMEM lane l owns entry l of the tile:
 //   score = s_j * sum_h (w_h / S_h) * ReLU(D_hi[h] + D_lo[h] / 16).
 //
-// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer and TMEM
-// owner, warps 2..5 = epilogue (TMEM lane groups 2,3,0,1).  Pipelines: an
-// 8-stage shared-memory ring of key tiles (full/empty mbarriers) and two TMEM
-// accumulator buffers (tmem_full/tmem_empty).  Every wait is bounded; a
+// Warp roles (320 threads): warp 0 = TMA producer, warp 1 = MMA issuer and TMEM
+// owner, warps 2..9 = two epilogue warpgroups that take alternate tiles (warp w
+// reads TMEM lane group w % 4).  Pipelines: an 8-stage shared-memory ring of key
+// tiles (full/empty mbarriers) and up to four TMEM accumulator buffers
+// (tmem_full/tmem_empty).  Every wait is bounded; a
 // timeout sets the workspace status word and all roles stop issuing work.
 // grid = (CTAs per query row, query rows); each CTA scores a contiguous range of
 // 128-entry tiles of one row, so its query operand is built once.
@@ -40,7 +41,8 @@ constexpr int kTileM = 128;
 constexpr int kDI = 128;
 constexpr int kStages = 8;
 constexpr int kStageBytes = kTileM * kDI;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kEpiGroups = 2;   // epilogue warpgroups; group e takes tiles it % 2 == e
 constexpr long long kWaitLimit = 1LL << 24;
 
 struct TcArgs {
@@ -140,8 +142,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
   uint64_t *full = reinterpret_cast<uint64_t *>(wq + 128);
   uint64_t *empty = full + kStages;
   uint64_t *tfull = empty + kStages;
-  uint64_t *tempty = tfull + 2;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
+  uint64_t *tempty = tfull + 4;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 4);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const CacheView &c = a.c;
@@ -159,15 +161,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
-    for (int s = 0; s < 2; ++s) { mbar_init(&tfull[s], 1); mbar_init(&tempty[s], 4); }
+    for (int s = 0; s < 4; ++s) { mbar_init(&tfull[s], 1); mbar_init(&tempty[s], 4); }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  const uint32_t ncols = H <= 32 ? 128u : (H <= 64 ? 256u : 512u);
+  const int n_acc = H <= 64 ? 4 : 2;                        // accumulator buffers (2H columns each)
+  const uint32_t ncols = H <= 32 ? 256u : 512u;
   uint32_t tmem = 0;
   if (warp != 0) {
-    // ---- query operand (warps 1..5, while warp 0 already streams keys): per-head
+    // ---- query operand (warps 1.., while warp 0 already streams keys): per-head
     //      power-of-two scale, exact e4m3 hi/lo split, written in the K-major
     //      128-byte-swizzle layout the MMA reads
     for (int h = warp - 1; h < H; h += kThreads / 32 - 1) {
@@ -203,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
       asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     tc_fence_before();
-    asm volatile("bar.sync 1, %0;" ::"n"(kThreads - 32) : "memory");   // warps 1..5 only
+    asm volatile("bar.sync 1, %0;" ::"n"(kThreads - 32) : "memory");   // all warps but the producer
     tc_fence_after();
     tmem = *tmem_slot;
   }
@@ -244,8 +247,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
       for (int it = 0; it < n_it; ++it) {
         const int s = it % kStages;
         const uint32_t ph = (uint32_t)(it / kStages) & 1u;
-        const int acc = it & 1;
-        const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+        const int acc = it % n_acc;
+        const uint32_t aph = (uint32_t)(it / n_acc) & 1u;
         if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, a.status)) break;
         if (!mbar_wait(&full[s], ph, abort_flag, a.status)) break;
         tc_fence_after();
@@ -263,36 +266,49 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
     }
   } else {   // ---- epilogue: TMEM lane group g = warp % 4 owns entries 32g .. 32g+31 of a tile
     const int g = warp & 3;
-    // key scales are read four tiles ahead so their memory latency overlaps the
-    // tiles in between instead of stalling each tile's epilogue
+    const int grp = (warp - 2) >> 2;   // epilogue group: tiles it with it % 2 == grp
+    // key scales are read four of this group's tiles ahead so their memory
+    // latency overlaps the tiles in between instead of stalling each epilogue
     auto scale_of = [&](int it2) -> float {
       const long long j2 = (tile_lo + it2) * kTileM + g * 32 + lane;
       return (it2 < n_it && j2 < n_vis) ? __ldg(c.idx_scale + entry_row(c, b, j2)) : 0.f;
     };
-    float sc0 = scale_of(0), sc1 = scale_of(1), sc2 = scale_of(2), sc3 = scale_of(3);
-    for (int it = 0; it < n_it; ++it) {
-      const int acc = it & 1;
-      const uint32_t aph = (uint32_t)(it >> 1) & 1u;
-      const bool ok = mbar_wait(&tfull[acc], aph, abort_flag, a.status);
-      if (!__all_sync(0xffffffffu, ok)) break;   // warp-uniform: the TMEM loads below are .sync.aligned
-      tc_fence_after();
-      const uint32_t taddr = tmem + ((uint32_t)(g * 32) << 16) + (uint32_t)(acc * 2 * H);
-      float sum = 0.f;
-      for (int c0 = 0; c0 < H; c0 += 32) {
-        uint32_t hv[32], lv[32];
-        tmem_ld32(taddr + c0, hv);
-        tmem_ld32(taddr + H + c0, lv);
-        tmem_wait_ld();
+    // slot u of sc[] holds the scale of this group's tile it0 + 2u; it is refilled
+    // in place four tiles ahead (no register shuffling that would wait on loads)
+    float sc[4];
 #pragma unroll
-        for (int h = 0; h < 32; ++h)
-          sum = fmaf(wq[c0 + h], fmaxf(fmaf(__uint_as_float(lv[h]), 0.0625f, __uint_as_float(hv[h])), 0.f), sum);
+    for (int u = 0; u < 4; ++u) sc[u] = scale_of(grp + 2 * u);
+    bool live = true;
+    for (int it0 = grp; it0 < n_it && live; it0 += 4 * kEpiGroups) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int it = it0 + kEpiGroups * u;
+        if (it >= n_it || !live) break;
+        const int acc = it % n_acc;
+        const uint32_t aph = (uint32_t)(it / n_acc) & 1u;
+        const bool ok = mbar_wait(&tfull[acc], aph, abort_flag, a.status);
+        if (!__all_sync(0xffffffffu, ok)) { live = false; break; }   // warp-uniform: TMEM loads are .sync.aligned
+        tc_fence_after();
+        const uint32_t taddr = tmem + ((uint32_t)(g * 32) << 16) + (uint32_t)(acc * 2 * H);
+        float s4[4] = {0.f, 0.f, 0.f, 0.f};   // independent partial sums (no 64-deep FMA chain)
+        for (int c0 = 0; c0 < H; c0 += 32) {
+          uint32_t hv[32], lv[32];
+          tmem_ld32(taddr + c0, hv);
+          tmem_ld32(taddr + H + c0, lv);
+          tmem_wait_ld();
+#pragma unroll
+          for (int h = 0; h < 32; ++h)
+            s4[h & 3] = fmaf(wq[c0 + h], fmaxf(fmaf(__uint_as_float(lv[h]), 0.0625f, __uint_as_float(hv[h])), 0.f),
+                             s4[h & 3]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+        const float sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+        const long long j = (tile_lo + it) * kTileM + g * 32 + lane;
+        if (j < n_vis) a.scores[(long long)row * a.stride + j] = sum * sc[u];
+        sc[u] = scale_of(it + 4 * kEpiGroups);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
-      const long long j = (tile_lo + it) * kTileM + g * 32 + lane;
-      if (j < n_vis) a.scores[(long long)row * a.stride + j] = sum * sc0;
-      sc0 = sc1; sc1 = sc2; sc2 = sc3; sc3 = scale_of(it + 4);
     }
   }
   __syncthreads();
@@ -328,7 +344,7 @@ bool index_tc_supported(const CacheView &c, int heads_idx) {
 }
 
 size_t index_tc_smem_bytes() {
-  return 1024 + (size_t)kStages * kStageBytes + 2 * 128 * kDI + 128 * sizeof(float) + (2 * kStages + 4) * 8 + 16;
+  return 1024 + (size_t)kStages * kStageBytes + 2 * 128 * kDI + 128 * sizeof(float) + (2 * kStages + 8) * 8 + 16;
 }
 
 cudaError_t launch_index_tc(const CacheView &c, int batch, int n_q, const void *q_idx, int q_dtype, const float *w,

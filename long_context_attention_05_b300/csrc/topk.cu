@@ -121,24 +121,29 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_row(CacheView c, int n_q,
 }
 
 // Cluster version: the CS CTAs of one thread-block cluster share a query row.
-// Each CTA keeps its slice of the row's keys in shared memory; per radix pass
-// each CTA builds the digit histogram of its slice and every CTA merges all CS
-// histograms through distributed shared memory (identical arithmetic in every
-// CTA, so all reach the same digit).  The compaction writes in index order: a
-// CTA's output offset is the count its lower-ranked peers select, and within a
-// CTA one block scan per 1024-key chunk orders the selected keys.
+// Each CTA keeps its slice of the row's keys in shared memory.  Three radix
+// passes (11, 11 and 10 bits): each CTA builds the digit histogram of its
+// slice; the cluster reduces it (CTA r sums bins of its own range over all
+// peers) and gathers the merged histogram back through distributed shared
+// memory, so every CTA holds the same histogram and reaches the same digit.
+// Histograms are double-buffered across passes, so a pass costs two cluster
+// barriers.  The compaction writes in index order: a CTA's output offset is
+// what its lower-ranked peers select; within a CTA each thread owns a
+// contiguous run of keys and one block scan orders them.
+constexpr int kBins = 2048;
+
 __global__ void __launch_bounds__(kTopkThreads) k_topk_cluster(CacheView c, int n_q, const float *scores,
                                                                long long stride, int k, int32_t *out_idx,
                                                                int32_t *out_count, int slice_cap) {
   namespace cg = cooperative_groups;
   cg::cluster_group cl = cg::this_cluster();
   extern __shared__ unsigned keys[];             // [slice_cap]
-  __shared__ unsigned hist[256];
+  __shared__ unsigned hist[2][kBins];            // this CTA's slice histogram (double-buffered)
+  __shared__ unsigned part[2][kBins];            // merged counts of this CTA's bin range
   __shared__ int scan_buf[64];
   __shared__ unsigned sh_prefix;
   __shared__ int sh_krem;
   __shared__ int cnt[2];                         // this CTA's (greater, equal) counts
-  __shared__ int merged[256];
   const int CS = (int)cl.num_blocks();
   const int rank = (int)cl.block_rank();
   const int row = blockIdx.y;
@@ -158,103 +163,106 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_cluster(CacheView c, int 
   const long long lo = min(n, rank * L), hi = min(n, lo + L);
   const int len = (int)(hi - lo);
   const float *s = scores + (long long)row * stride + lo;
-  for (int j = threadIdx.x; j < len; j += blockDim.x) keys[j] = float_key(__ldg(s + j));
+  // eight loads in flight per thread per round (not one memory round trip per key)
+  for (int j0 = 0; j0 < len; j0 += 8 * kTopkThreads) {
+    float v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int j = j0 + q * kTopkThreads + (int)threadIdx.x;
+      v[q] = j < len ? __ldg(s + j) : 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int j = j0 + q * kTopkThreads + (int)threadIdx.x;
+      if (j < len) keys[j] = float_key(v[q]);
+    }
+  }
+  const int per = kBins / CS;                    // bins this CTA reduces
   unsigned prefix = 0, mask = 0;
   int krem = k;
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    for (int e = threadIdx.x; e < 256; e += blockDim.x) hist[e] = 0;
+  const int shifts[3] = {21, 10, 0};
+  const int widths[3] = {11, 11, 10};
+  for (int pass = 0; pass < 3; ++pass) {
+    const int shift = shifts[pass];
+    const unsigned dmask = (1u << widths[pass]) - 1u;
+    unsigned *h = hist[pass & 1];
+    unsigned *pm = part[pass & 1];
+    for (int e = threadIdx.x; e < kBins; e += blockDim.x) h[e] = 0;
     __syncthreads();
     for (int j = threadIdx.x; j < len; j += blockDim.x) {
       const unsigned key = keys[j];
       const bool in = (key & mask) == prefix;
-      const unsigned bin = (key >> shift) & 255u;
+      const unsigned bin = (key >> shift) & dmask;
       const unsigned act = __ballot_sync(__activemask(), in);
       if (in) {
         const unsigned peers = __match_any_sync(act, bin);
-        if ((threadIdx.x & 31) == (unsigned)(__ffs(peers) - 1)) atomicAdd(&hist[bin], __popc(peers));
+        if ((threadIdx.x & 31) == (unsigned)(__ffs(peers) - 1)) atomicAdd(&h[bin], __popc(peers));
       }
     }
-    cl.sync();   // every slice histogram complete and visible to the cluster
-    if (threadIdx.x < 256) {
-      int cdig = 0;
-      for (int r = 0; r < CS; ++r) cdig += (int)cl.map_shared_rank(hist, r)[threadIdx.x];
-      merged[threadIdx.x] = cdig;
+    cl.sync();   // all slice histograms complete
+    for (int e = threadIdx.x; e < per; e += blockDim.x) {
+      unsigned v[16];
+#pragma unroll
+      for (int r = 0; r < 16; ++r) v[r] = r < CS ? cl.map_shared_rank(h, r)[rank * per + e] : 0u;   // all in flight
+      unsigned sum = 0;
+#pragma unroll
+      for (int r = 0; r < 16; ++r) sum += v[r];
+      pm[rank * per + e] = sum;
+    }
+    cl.sync();   // every CTA's merged range complete
+    // gather the merged histogram; thread x owns bins 2047-2x and 2046-2x (descending)
+    const int b0 = kBins - 1 - 2 * (int)threadIdx.x, b1 = b0 - 1;
+    const unsigned c0 = cl.map_shared_rank(pm, b0 / per)[b0];
+    const unsigned c1 = cl.map_shared_rank(pm, b1 / per)[b1];
+    int tot;
+    const int above = block_exclusive_scan((int)(c0 + c1), scan_buf, tot);   // keys in higher bins
+    if (above < krem && above + (int)(c0 + c1) >= krem) {
+      const bool first = above + (int)c0 >= krem;
+      sh_prefix = prefix | ((unsigned)(first ? b0 : b1) << shift);
+      sh_krem = krem - (first ? above : above + (int)c0);
     }
     __syncthreads();
-    if (threadIdx.x < 32) {
-      // lane l owns bins 255-8l .. 248-8l (descending); find the bin where the
-      // count of larger keys reaches krem
-      int part = 0;
-      for (int q = 0; q < 8; ++q) part += merged[255 - 8 * threadIdx.x - q];
-      int incl = part;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if ((int)threadIdx.x >= o) incl += y;
-      }
-      const int before = incl - part;
-      if (before < krem && incl >= krem) {
-        int cum = before;
-        for (int q = 0; q < 8; ++q) {
-          const int dgt = 255 - 8 * threadIdx.x - q;
-          if (cum + merged[dgt] >= krem) {
-            sh_prefix = prefix | ((unsigned)dgt << shift);
-            sh_krem = krem - cum;
-            break;
-          }
-          cum += merged[dgt];
-        }
-      }
-    }
-    cl.sync();   // peers are done reading this CTA's histogram; digit published
     prefix = sh_prefix;
     krem = sh_krem;
-    mask |= 255u << shift;
+    mask |= dmask << shift;
   }
-  // counts of this slice
+  // prefix = T, the k-th largest key; krem keys equal to T are still to be taken
+  const int seg = (len + (int)blockDim.x - 1) / (int)blockDim.x;
+  const int a0 = min(len, (int)threadIdx.x * seg), a1 = min(len, a0 + seg);
   int gt = 0, eq = 0;
-  for (int j = threadIdx.x; j < len; j += blockDim.x) {
+  for (int j = a0; j < a1; ++j) {
     gt += keys[j] > prefix;
     eq += keys[j] == prefix;
   }
-  int tg, te;
-  block_exclusive_scan(gt, scan_buf, tg);
-  block_exclusive_scan(eq, scan_buf, te);
-  if (threadIdx.x == 0) { cnt[0] = tg; cnt[1] = te; }
+  int tot;
+  const int ex = block_exclusive_scan((eq << 16) | gt, scan_buf, tot);   // per CTA: counts < 2^16
+  if (threadIdx.x == 0) { cnt[0] = tot & 0xFFFF; cnt[1] = tot >> 16; }
   cl.sync();
   long long base = 0;
   int eq_before = 0;
-  for (int r = 0; r < rank; ++r) {
-    const int *pc = cl.map_shared_rank(cnt, r);
-    const int g_r = pc[0], e_r = pc[1];
-    base += g_r + max(0, min(e_r, krem - eq_before));
-    eq_before += e_r;
+  int pg[16], pe[16];
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    pg[r] = r < rank ? cl.map_shared_rank(cnt, r)[0] : 0;
+    pe[r] = r < rank ? cl.map_shared_rank(cnt, r)[1] : 0;
   }
-  int limit = max(0, krem - eq_before);   // equal keys this CTA may still take, in index order
-  const int lane = threadIdx.x & 31;
-  const unsigned lt = (1u << lane) - 1u;
-  for (int c0 = 0; c0 < len; c0 += blockDim.x) {
-    const int j = c0 + threadIdx.x;
-    const bool valid = j < len;
-    const unsigned key = valid ? keys[j] : 0u;
-    const bool isg = valid && key > prefix, ise = valid && key == prefix;
-    const unsigned bg = __ballot_sync(0xffffffffu, isg), be = __ballot_sync(0xffffffffu, ise);
-    const int packed = (int)(((unsigned)__popc(be) << 16) | (unsigned)__popc(bg));
-    int tot;
-    const int ex = block_exclusive_scan(lane == 0 ? packed : 0, scan_buf, tot);
-    const int wex = __shfl_sync(0xffffffffu, ex, 0);
-    const int G_w = wex & 0xFFFF, E_w = wex >> 16;
-    const int erank = E_w + __popc(be & lt);
-    const bool take = isg || (ise && erank < limit);
-    const unsigned bt = __ballot_sync(0xffffffffu, take);
-    if (take) {
-      const long long pos = base + G_w + min(limit, E_w) + __popc(bt & lt);
-      out[pos] = (int32_t)(lo + j);
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    base += pg[r] + max(0, min(pe[r], krem - eq_before));
+    eq_before += pe[r];
+  }
+  const int limit = max(0, krem - eq_before);   // equal keys this CTA may take, in index order
+  const int g_before = ex & 0xFFFF, e_before = ex >> 16;
+  long long pos = base + g_before + min(limit, e_before);
+  int e_seen = e_before;
+  for (int j = a0; j < a1; ++j) {
+    const unsigned key = keys[j];
+    if (key > prefix) {
+      out[pos++] = (int32_t)(lo + j);
+    } else if (key == prefix) {
+      if (e_seen < limit) out[pos++] = (int32_t)(lo + j);
+      ++e_seen;
     }
-    const int G = tot & 0xFFFF, E = tot >> 16;
-    base += G + min(limit, E);
-    limit -= min(limit, E);
   }
   if (rank == 0 && threadIdx.x == 0) out_count[row] = k;
   cl.sync();   // no CTA leaves while a peer may still read its shared memory
@@ -273,7 +281,7 @@ cudaError_t launch_topk(const CacheView &c, int batch, int n_q, const float *sco
   }
   const long long slice = (n_cap + cs - 1) / cs;
   const size_t smem = (size_t)slice * sizeof(unsigned);
-  if (smem > 160 * 1024) {
+  if (smem > 160 * 1024 || cs > 16 || kBins % cs) {
     k_topk_row<<<rows, kTopkThreads, 0, st>>>(c, n_q, scores, stride, k, out_idx, out_count);
     return cudaGetLastError();
   }
