@@ -65,6 +65,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttendArgs a) {
   constexpr int LDS = kKeys + 4;             // fp32 row stride of the logit tile
   constexpr int DQ = D / 4;                  // dims per warp in the value phase
   constexpr int NT = DQ / 8;                 // n-tiles per warp in the value phase
+  constexpr int kGatherPer = (kKeys * ((D - 64) / 16 > D / 8 - 8 ? (D - 64) / 16 + 8 : D / 8) + kThreads - 1) / kThreads;
   extern __shared__ __align__(16) uint8_t smem[];
   __half *Qs = reinterpret_cast<__half *>(smem);                        // [64][LDQ]
   __half *Ks = Qs + kHeadsMax * LDQ;                                     // [64][LDQ]
@@ -105,36 +106,138 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttendArgs a) {
     }
     return src;
   };
-  const long long ch0 = (long long)split * a.chunks_per_split;
-  // the first chunk's key lookups go out before the query work, to overlap
-  long long src_next = -1;
-  float sig_next = 0.f;
-  if (tid < kKeys && ch0 * kKeys < U) {
-    src_next = key_src(ch0 * kKeys);
-    sig_next = src_next >= 0 ? 256.f * __ldg(c.kv_scale + src_next) : (src_next <= -2 ? 1.f : 0.f);
-  }
+  // ---- gather of a chunk's key tile as f16, in 16-byte pieces: gather_load issues
+  //      every load of this thread into registers, gather_store converts and stores
+  constexpr int NOPE16 = DN / 16;   // 16-byte e4m3 pieces per entry
+  constexpr int ROPE16 = 64 / 8;    // 16-byte bf16 pieces of the rotary dims
+  constexpr int RAW16 = D / 8;      // 16-byte bf16 pieces of a raw window token
+  constexpr int PIECES = NOPE16 > RAW16 - ROPE16 ? NOPE16 + ROPE16 : RAW16;
+  auto gather_load = [&](uint4 (&buf)[kGatherPer]) {
+#pragma unroll
+    for (int r = 0; r < kGatherPer; ++r) {
+      const int x = tid + r * kThreads;
+      buf[r] = make_uint4(0, 0, 0, 0);
+      if (x < kKeys * PIECES) {
+        const int kk = x / PIECES, p = x % PIECES;
+        const long long src = ksrc[kk];
+        if (src >= 0) {
+          if (p < NOPE16) buf[r] = __ldg(reinterpret_cast<const uint4 *>(c.kv_nope + src * DN) + p);
+          else if (p < NOPE16 + ROPE16)
+            buf[r] = __ldg(reinterpret_cast<const uint4 *>(c.kv_rope + src * 64 * 2) + (p - NOPE16));
+        } else if (src <= -2 && p < RAW16) {
+          const long long tau = -2 - src;
+          buf[r] = __ldg(reinterpret_cast<const uint4 *>(c.win + ((long long)b * c.win_cap + tau % c.win_cap) * D * 2) + p);
+        }
+      }
+    }
+  };
+  auto gather_store = [&](const uint4 (&buf)[kGatherPer]) {
+#pragma unroll
+    for (int r = 0; r < kGatherPer; ++r) {
+      const int x = tid + r * kThreads;
+      if (x >= kKeys * PIECES) continue;
+      const int kk = x / PIECES, p = x % PIECES;
+      const long long src = ksrc[kk];
+      __half *dst = Ks + kk * LDQ;
+      const uint4 u = buf[r];
+      if (src >= 0) {
+        if (p < NOPE16) {
+          uint4 o0, o1;
+          o0.x = e4m3x2_to_f16x2_scaled(u.x); o0.y = e4m3x2_to_f16x2_scaled(u.x >> 16);
+          o0.z = e4m3x2_to_f16x2_scaled(u.y); o0.w = e4m3x2_to_f16x2_scaled(u.y >> 16);
+          o1.x = e4m3x2_to_f16x2_scaled(u.z); o1.y = e4m3x2_to_f16x2_scaled(u.z >> 16);
+          o1.z = e4m3x2_to_f16x2_scaled(u.w); o1.w = e4m3x2_to_f16x2_scaled(u.w >> 16);
+          *reinterpret_cast<uint4 *>(dst + p * 16) = o0;
+          *reinterpret_cast<uint4 *>(dst + p * 16 + 8) = o1;
+        } else if (p < NOPE16 + ROPE16) {
+          const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+          uint4 o;
+          uint32_t *op = &o.x;
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            op[e] = pack_h2(bf16_bits_to_f32((uint16_t)(w4[e] & 0xFFFF)), bf16_bits_to_f32((uint16_t)(w4[e] >> 16)));
+          *reinterpret_cast<uint4 *>(dst + DN + (p - NOPE16) * 8) = o;
+        }
+      } else if (src <= -2) {
+        if (p < RAW16) {
+          const long long tau = -2 - src;
+          const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+          float f[8];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            f[2 * e] = bf16_bits_to_f32((uint16_t)(w4[e] & 0xFFFF));
+            f[2 * e + 1] = bf16_bits_to_f32((uint16_t)(w4[e] >> 16));
+          }
+          if (p * 8 >= DN) {   // rotary dims of a window token turn at its position
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+              float cs, sn;
+              rope_cos_sin(tau, a.rope.step[(p * 8 + e - DN) >> 1], cs, sn);
+              const float x0 = f[e], x1 = f[e + 1];
+              f[e] = fmaf(x0, cs, -x1 * sn);
+              f[e + 1] = fmaf(x0, sn, x1 * cs);
+            }
+          }
+          uint4 o;
+          o.x = pack_h2(f[0], f[1]); o.y = pack_h2(f[2], f[3]);
+          o.z = pack_h2(f[4], f[5]); o.w = pack_h2(f[6], f[7]);
+          *reinterpret_cast<uint4 *>(dst + p * 8) = o;
+        }
+      } else if (p < RAW16) {
+        *reinterpret_cast<uint4 *>(dst + p * 8) = make_uint4(0, 0, 0, 0);
+      }
+    }
+  };
 
+  const long long ch0 = (long long)split * a.chunks_per_split;
+  // prologue: every independent memory access of the first chunk goes out before
+  // any conversion work -- the first chunk's key lookups, the query rows, then
+  // (once the key rows are known) the key gather
+  long long src_next = -1;
+  float sig_next = 0.f, scale_first = 0.f;
+  if (tid < kKeys) {
+    const long long src = ch0 * kKeys < U ? key_src(ch0 * kKeys) : -1;
+    ksrc[tid] = src;
+    if (src >= 0) scale_first = __ldg(c.kv_scale + src);   // consumed after the query work
+    sig[tid] = src <= -2 ? 1.f : 0.f;
+  }
   // ---- query: one (cos, sin) per rotary pair at t, shared by all heads
   if (tid < 32) {
     float cs, sn;
     rope_cos_sin(t, a.rope.step[tid], cs, sn);
     qcs[tid] = make_float2(cs, sn);
   }
-  __syncthreads();
-  // warp w converts heads w, w+16, ...; lane holds D/32 consecutive dims
+  // warp w converts heads w, w+16, ...; lane holds D/32 consecutive dims.  The
+  // 16-byte query loads of all of a warp's heads are issued first.
+  constexpr int QH = kHeadsMax / (kThreads / 32);          // heads per warp
+  constexpr int QV = (D / 32) % 8 == 0 ? (D / 32) / 8 : 1;  // 16-byte pieces per lane per head
+  uint4 qraw[QH][QV];
+  if (a.q_dtype == CSA_BF16 && (D / 32) % 8 == 0) {
+#pragma unroll
+    for (int hh = 0; hh < QH; ++hh) {
+      const int h = warp + hh * (kThreads / 32);
+#pragma unroll
+      for (int u = 0; u < QV; ++u)
+        qraw[hh][u] = h < H ? __ldg(reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(a.q) +
+                                                                     ((long long)row * H + h) * D + lane * (D / 32)) + u)
+                            : make_uint4(0, 0, 0, 0);
+    }
+  }
+  __syncthreads();   // ksrc, qcs visible
+  uint4 gbuf[kGatherPer];
+  gather_load(gbuf);
   {
     constexpr int PER = D / 32;
 #pragma unroll
-    for (int hh = 0; hh < kHeadsMax / (kThreads / 32); ++hh) {
+    for (int hh = 0; hh < QH; ++hh) {
       const int h = warp + hh * (kThreads / 32);
       float v[PER];
       if (h < H) {
         const long long q0 = ((long long)row * H + h) * D + lane * PER;
-        if (a.q_dtype == CSA_BF16 && PER % 8 == 0) {   // 16-byte loads
-          const uint4 *src = reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(a.q) + q0);
+        if (a.q_dtype == CSA_BF16 && PER % 8 == 0) {   // from the 16-byte loads issued above
 #pragma unroll
           for (int u = 0; u < PER / 8; ++u) {
-            const uint4 x = __ldg(src + u);
+            const uint4 x = qraw[hh][u];
             const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -185,6 +288,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttendArgs a) {
     }
   }
 
+  if (tid < kKeys) {
+    if (ksrc[tid] >= 0) sig[tid] = 256.f * scale_first;
+    // look up the next chunk's keys now; used one chunk later
+    const long long u1 = (ch0 + 1) * kKeys;
+    if (a.chunks_per_split > 1 && u1 < U) {
+      src_next = key_src(u1);
+      sig_next = src_next >= 0 ? 256.f * __ldg(c.kv_scale + src_next) : (src_next <= -2 ? 1.f : 0.f);
+    }
+  }
+  gather_store(gbuf);
+
   float acc[NT][4];
 #pragma unroll
   for (int n = 0; n < NT; ++n)
@@ -194,103 +308,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttendArgs a) {
   for (long long chunk = ch0; chunk < ch0 + a.chunks_per_split; ++chunk) {
     const long long u0 = chunk * kKeys;
     if (u0 >= U) break;
-    __syncthreads();   // previous chunk's value phase is done with Ks / P
-    if (tid < kKeys) {
-      ksrc[tid] = src_next;
-      sig[tid] = sig_next;
-      // look up the next chunk's keys now; used one chunk later
-      const long long u1 = u0 + kKeys;
-      src_next = -1;
-      sig_next = 0.f;
-      if (chunk + 1 < ch0 + a.chunks_per_split && u1 < U) {
-        src_next = key_src(u1);
-        sig_next = src_next >= 0 ? 256.f * __ldg(c.kv_scale + src_next) : (src_next <= -2 ? 1.f : 0.f);
-      }
-    }
-    __syncthreads();
-    // ---- gather the key tile as f16, in 16-byte pieces: every thread first issues
-    //      all of its loads, then converts and stores (one memory latency per chunk)
-    {
-      constexpr int NOPE16 = DN / 16;   // 16-byte e4m3 pieces per entry
-      constexpr int ROPE16 = 64 / 8;    // 16-byte bf16 pieces of the rotary dims
-      constexpr int RAW16 = D / 8;      // 16-byte bf16 pieces of a raw window token
-      constexpr int PIECES = NOPE16 > RAW16 - ROPE16 ? NOPE16 + ROPE16 : RAW16;
-      constexpr int PER_T = (kKeys * PIECES + kThreads - 1) / kThreads;
-      uint4 buf[PER_T];
-#pragma unroll
-      for (int r = 0; r < PER_T; ++r) {
-        const int x = tid + r * kThreads;
-        buf[r] = make_uint4(0, 0, 0, 0);
-        if (x < kKeys * PIECES) {
-          const int kk = x / PIECES, p = x % PIECES;
-          const long long src = ksrc[kk];
-          if (src >= 0) {
-            if (p < NOPE16) buf[r] = __ldg(reinterpret_cast<const uint4 *>(c.kv_nope + src * DN) + p);
-            else if (p < NOPE16 + ROPE16)
-              buf[r] = __ldg(reinterpret_cast<const uint4 *>(c.kv_rope + src * 64 * 2) + (p - NOPE16));
-          } else if (src <= -2 && p < RAW16) {
-            const long long tau = -2 - src;
-            buf[r] = __ldg(reinterpret_cast<const uint4 *>(c.win + ((long long)b * c.win_cap + tau % c.win_cap) * D * 2) + p);
-          }
+    __syncthreads();   // previous chunk's value phase is done with Ks / P (first chunk: its tile is stored)
+    if (chunk != ch0) {
+      if (tid < kKeys) {
+        ksrc[tid] = src_next;
+        sig[tid] = sig_next;
+        const long long u1 = u0 + kKeys;
+        src_next = -1;
+        sig_next = 0.f;
+        if (chunk + 1 < ch0 + a.chunks_per_split && u1 < U) {
+          src_next = key_src(u1);
+          sig_next = src_next >= 0 ? 256.f * __ldg(c.kv_scale + src_next) : (src_next <= -2 ? 1.f : 0.f);
         }
       }
-#pragma unroll
-      for (int r = 0; r < PER_T; ++r) {
-        const int x = tid + r * kThreads;
-        if (x >= kKeys * PIECES) continue;
-        const int kk = x / PIECES, p = x % PIECES;
-        const long long src = ksrc[kk];
-        __half *dst = Ks + kk * LDQ;
-        const uint4 u = buf[r];
-        if (src >= 0) {
-          if (p < NOPE16) {
-            uint4 o0, o1;
-            o0.x = e4m3x2_to_f16x2_scaled(u.x); o0.y = e4m3x2_to_f16x2_scaled(u.x >> 16);
-            o0.z = e4m3x2_to_f16x2_scaled(u.y); o0.w = e4m3x2_to_f16x2_scaled(u.y >> 16);
-            o1.x = e4m3x2_to_f16x2_scaled(u.z); o1.y = e4m3x2_to_f16x2_scaled(u.z >> 16);
-            o1.z = e4m3x2_to_f16x2_scaled(u.w); o1.w = e4m3x2_to_f16x2_scaled(u.w >> 16);
-            *reinterpret_cast<uint4 *>(dst + p * 16) = o0;
-            *reinterpret_cast<uint4 *>(dst + p * 16 + 8) = o1;
-          } else if (p < NOPE16 + ROPE16) {
-            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-            uint4 o;
-            uint32_t *op = &o.x;
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              op[e] = pack_h2(bf16_bits_to_f32((uint16_t)(w4[e] & 0xFFFF)), bf16_bits_to_f32((uint16_t)(w4[e] >> 16)));
-            *reinterpret_cast<uint4 *>(dst + DN + (p - NOPE16) * 8) = o;
-          }
-        } else if (src <= -2) {
-          if (p < RAW16) {
-            const long long tau = -2 - src;
-            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-            float f[8];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              f[2 * e] = bf16_bits_to_f32((uint16_t)(w4[e] & 0xFFFF));
-              f[2 * e + 1] = bf16_bits_to_f32((uint16_t)(w4[e] >> 16));
-            }
-            if (p * 8 >= DN) {   // rotary dims of a window token turn at its position
-#pragma unroll
-              for (int e = 0; e < 8; e += 2) {
-                float cs, sn;
-                rope_cos_sin(tau, a.rope.step[(p * 8 + e - DN) >> 1], cs, sn);
-                const float x0 = f[e], x1 = f[e + 1];
-                f[e] = fmaf(x0, cs, -x1 * sn);
-                f[e + 1] = fmaf(x0, sn, x1 * cs);
-              }
-            }
-            uint4 o;
-            o.x = pack_h2(f[0], f[1]); o.y = pack_h2(f[2], f[3]);
-            o.z = pack_h2(f[4], f[5]); o.w = pack_h2(f[6], f[7]);
-            *reinterpret_cast<uint4 *>(dst + p * 8) = o;
-          }
-        } else if (p < RAW16) {
-          *reinterpret_cast<uint4 *>(dst + p * 8) = make_uint4(0, 0, 0, 0);
-        }
-      }
+      __syncthreads();
+      gather_load(gbuf);
+      gather_store(gbuf);
+      __syncthreads();
     }
-    __syncthreads();
     // ---- logits: warp (g, qq): heads 16g..16g+15 x keys 16qq..16qq+15
     if (16 * g < H) {
       float sn[2][4] = {}, sr[2][4] = {};

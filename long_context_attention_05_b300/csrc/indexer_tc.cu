@@ -11,13 +11,14 @@
 //
 // Design.  The e4m3 keys stream from HBM once, by TMA, straight into the tensor
 // cores: D[entry, head] = sum_k code[entry, k] * q'[head, k] with
-// tcgen05.mma kind::f8f6f4, M = 128 entries (one TMEM lane each), N = heads,
-// K = 128 (four K=32 steps over one 128-byte swizzled row).  The bf16 query is
+// tcgen05.mma kind::f8f6f4, M = 128 entries (one TMEM lane each), N = 2 x heads
+// (the hi and lo query operands stacked), K = 128 (four K=32 steps over one
+// 128-byte swizzled row).  The bf16 query is
 // made an exact pair of e4m3 operands: per head a power of two S_h puts
 // max|q_h| below 2^8, hi = e4m3(q*S_h), lo = e4m3((q*S_h - hi) * 16); for every
 // component with |q*S_h| >= 2^-6 this is exact (8 significant bits = 4 + 4), so
 // the product q . code is the bf16 query's product up to fp32 accumulation.
-// Two accumulators (hi, lo) per tile, double-buffered in TMEM (4*heads columns).
+// Per tile one accumulator of 2*heads columns (hi | lo); up to four in TMEM.
 // The epilogue thread of TMEM lane l owns entry l of the tile:
 //   score = s_j * sum_h (w_h / S_h) * ReLU(D_hi[h] + D_lo[h] / 16).
 //
@@ -136,9 +137,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint8_t *stage = base;                                   // kStages x 16 KB key tiles
-  uint8_t *bhi = base + kStages * kStageBytes;             // [heads][128] e4m3, swizzled
-  uint8_t *blo = bhi + 128 * kDI;
-  float *wq = reinterpret_cast<float *>(blo + 128 * kDI);  // [heads] w_h / S_h
+  uint8_t *bhi = base + kStages * kStageBytes;             // [heads][128] e4m3 hi, swizzled
+  uint8_t *blo = bhi + a.heads * kDI;                      // [heads][128] e4m3 lo, right after:
+                                                           // one N = 2*heads operand
+  float *wq = reinterpret_cast<float *>(bhi + 2 * 128 * kDI);  // [heads] w_h / S_h
   uint64_t *full = reinterpret_cast<uint64_t *>(wq + 128);
   uint64_t *empty = full + kStages;
   uint64_t *tfull = empty + kStages;
@@ -242,8 +244,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
     }
   } else if (warp == 1) {
     if (lane == 0) {   // ---- MMA issuer
-      const uint32_t idesc = (1u << 4) | ((uint32_t)(H >> 3) << 17) | ((uint32_t)(kTileM >> 4) << 24);
-      const uint32_t bh = su32(bhi), bl = su32(blo);
+      // one MMA per K step: N = 2H columns, hi heads in [0, H), lo heads in [H, 2H)
+      const uint32_t idesc = (1u << 4) | ((uint32_t)((2 * H) >> 3) << 17) | ((uint32_t)(kTileM >> 4) << 24);
+      const uint32_t bh = su32(bhi);
       for (int it = 0; it < n_it; ++it) {
         const int s = it % kStages;
         const uint32_t ph = (uint32_t)(it / kStages) & 1u;
@@ -253,13 +256,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
         if (!mbar_wait(&full[s], ph, abort_flag, a.status)) break;
         tc_fence_after();
         const uint32_t as = su32(stage + s * kStageBytes);
-        const uint32_t d_hi = tmem + (uint32_t)(acc * 2 * H), d_lo = d_hi + (uint32_t)H;
+        const uint32_t d = tmem + (uint32_t)(acc * 2 * H);
 #pragma unroll
-        for (int kk = 0; kk < kDI / 32; ++kk) {
-          const uint64_t ad = sw128_desc(as + kk * 32);
-          umma_f8(d_hi, ad, sw128_desc(bh + kk * 32), idesc, kk > 0);
-          umma_f8(d_lo, ad, sw128_desc(bl + kk * 32), idesc, kk > 0);
-        }
+        for (int kk = 0; kk < kDI / 32; ++kk)
+          umma_f8(d, sw128_desc(as + kk * 32), sw128_desc(bh + kk * 32), idesc, kk > 0);
         umma_commit(&empty[s]);
         umma_commit(&tfull[acc]);
       }

@@ -226,16 +226,24 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_cluster(CacheView c, int 
     krem = sh_krem;
     mask |= dmask << shift;
   }
-  // prefix = T, the k-th largest key; krem keys equal to T are still to be taken
-  const int seg = (len + (int)blockDim.x - 1) / (int)blockDim.x;
-  const int a0 = min(len, (int)threadIdx.x * seg), a1 = min(len, a0 + seg);
-  int gt = 0, eq = 0;
-  for (int j = a0; j < a1; ++j) {
-    gt += keys[j] > prefix;
-    eq += keys[j] == prefix;
+  // prefix = T, the k-th largest key; krem keys equal to T are still to be taken.
+  // Warp w owns the contiguous run [w*seg, (w+1)*seg) of this slice and walks it
+  // 32 keys at a time (coalesced, conflict-free); ballots order keys inside a
+  // round, one block scan orders the warps.
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = (int)blockDim.x >> 5;
+  const unsigned lt = (1u << lane) - 1u;
+  const int seg = ((len + nwarps - 1) / nwarps + 31) & ~31;
+  const int w0 = min(len, warp * seg), w1 = min(len, w0 + seg);
+  int gw = 0, ew = 0;   // this warp's counts of keys > T and == T
+  for (int j0 = w0; j0 < w1; j0 += 32) {
+    const int j = j0 + lane;
+    const unsigned key = j < w1 ? keys[j] : 0u;
+    gw += __popc(__ballot_sync(0xffffffffu, j < w1 && key > prefix));
+    ew += __popc(__ballot_sync(0xffffffffu, j < w1 && key == prefix));
   }
   int tot;
-  const int ex = block_exclusive_scan((eq << 16) | gt, scan_buf, tot);   // per CTA: counts < 2^16
+  const int ex = block_exclusive_scan(lane == 0 ? ((ew << 16) | gw) : 0, scan_buf, tot);   // counts < 2^16
+  const int wex = __shfl_sync(0xffffffffu, ex, 0);
   if (threadIdx.x == 0) { cnt[0] = tot & 0xFFFF; cnt[1] = tot >> 16; }
   cl.sync();
   long long base = 0;
@@ -252,17 +260,18 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_cluster(CacheView c, int 
     eq_before += pe[r];
   }
   const int limit = max(0, krem - eq_before);   // equal keys this CTA may take, in index order
-  const int g_before = ex & 0xFFFF, e_before = ex >> 16;
-  long long pos = base + g_before + min(limit, e_before);
-  int e_seen = e_before;
-  for (int j = a0; j < a1; ++j) {
-    const unsigned key = keys[j];
-    if (key > prefix) {
-      out[pos++] = (int32_t)(lo + j);
-    } else if (key == prefix) {
-      if (e_seen < limit) out[pos++] = (int32_t)(lo + j);
-      ++e_seen;
-    }
+  int e_seen = wex >> 16;                        // equal keys before this warp's run (in this CTA)
+  long long pos = base + (wex & 0xFFFF) + min(limit, e_seen);
+  for (int j0 = w0; j0 < w1; j0 += 32) {
+    const int j = j0 + lane;
+    const unsigned key = j < w1 ? keys[j] : 0u;
+    const bool isg = j < w1 && key > prefix, ise = j < w1 && key == prefix;
+    const unsigned be = __ballot_sync(0xffffffffu, ise);
+    const bool take = isg || (ise && e_seen + __popc(be & lt) < limit);
+    const unsigned bt = __ballot_sync(0xffffffffu, take);
+    if (take) out[pos + __popc(bt & lt)] = (int32_t)(lo + j);
+    pos += __popc(bt);
+    e_seen += __popc(be);
   }
   if (rank == 0 && threadIdx.x == 0) out_count[row] = k;
   cl.sync();   // no CTA leaves while a peer may still read its shared memory
