@@ -35,6 +35,8 @@ __global__ void __launch_bounds__(kAttThreads) k_attend(AttendArgs a) {
 
   const int row = blockIdx.z;
   const int b = row / a.n_q, iq = row % a.n_q;
+  pdl_wait();
+  pdl_trigger();
   const long long t = c.n_tokens[b] - a.n_q + iq;
   const long long n_vis = min((t + 1) / c.m, c.cap);
   const long long n_list = a.idx ? a.k : n_vis;
@@ -197,6 +199,8 @@ __global__ void __launch_bounds__(256) k_attend_combine(AttendArgs a) {
   __shared__ float sh_M, sh_L;
   const int h = blockIdx.x, row = blockIdx.y;
   const int d = a.c.d, S = a.n_splits;
+  pdl_wait();
+  pdl_trigger();
   const float z = __ldg(a.sink + h);
   const long long base = (long long)row * S * a.heads + h;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -272,15 +276,13 @@ cudaError_t launch_attend(const AttendArgs &a0, int rows, cudaStream_t st) {
   const size_t smem = attend_smem_bytes(a.c.d);
   cudaFuncSetAttribute(k_attend, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   dim3 grid(a.n_splits, (a.heads + kHG - 1) / kHG, rows);
-  k_attend<<<grid, kAttThreads, smem, st>>>(a);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(k_attend, grid, dim3(kAttThreads), smem, st, 1, a);
   if (e != cudaSuccess || a.n_splits == 1) return e;
   return launch_attend_combine(a, rows, st);
 }
 
 cudaError_t launch_attend_combine(const AttendArgs &a, int rows, cudaStream_t st) {
-  k_attend_combine<<<dim3(a.heads, rows), 256, a.n_splits * sizeof(float), st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(k_attend_combine, dim3(a.heads, rows), dim3(256), a.n_splits * sizeof(float), st, 1, a);
 }
 
 }  // namespace csa

@@ -190,11 +190,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttendArgs a) {
   };
 
   const long long ch0 = (long long)split * a.chunks_per_split;
+  constexpr int QH = kHeadsMax / (kThreads / 32);          // heads per warp
+  constexpr int QV = (D / 32) % 8 == 0 ? (D / 32) / 8 : 1;  // 16-byte pieces per lane per head
+  uint4 qraw[QH][QV];
   // prologue: every independent memory access of the first chunk goes out before
   // any conversion work -- the first chunk's key lookups, the query rows, then
   // (once the key rows are known) the key gather
   long long src_next = -1;
   float sig_next = 0.f, scale_first = 0.f;
+  // the query rows and n_tokens are ready before this kernel starts; the key
+  // indices come from the kernel just before it
+  if (a.q_dtype == CSA_BF16 && (D / 32) % 8 == 0) {
+#pragma unroll
+    for (int hh = 0; hh < QH; ++hh) {
+      const int h = warp + hh * (kThreads / 32);
+#pragma unroll
+      for (int u = 0; u < QV; ++u)
+        qraw[hh][u] = h < H ? __ldg(reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(a.q) +
+                                                                     ((long long)row * H + h) * D + lane * (D / 32)) + u)
+                            : make_uint4(0, 0, 0, 0);
+    }
+  }
+  pdl_wait();
+  pdl_trigger();
   if (tid < kKeys) {
     const long long src = ch0 * kKeys < U ? key_src(ch0 * kKeys) : -1;
     ksrc[tid] = src;
@@ -207,22 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttendArgs a) {
     rope_cos_sin(t, a.rope.step[tid], cs, sn);
     qcs[tid] = make_float2(cs, sn);
   }
-  // warp w converts heads w, w+16, ...; lane holds D/32 consecutive dims.  The
-  // 16-byte query loads of all of a warp's heads are issued first.
-  constexpr int QH = kHeadsMax / (kThreads / 32);          // heads per warp
-  constexpr int QV = (D / 32) % 8 == 0 ? (D / 32) / 8 : 1;  // 16-byte pieces per lane per head
-  uint4 qraw[QH][QV];
-  if (a.q_dtype == CSA_BF16 && (D / 32) % 8 == 0) {
-#pragma unroll
-    for (int hh = 0; hh < QH; ++hh) {
-      const int h = warp + hh * (kThreads / 32);
-#pragma unroll
-      for (int u = 0; u < QV; ++u)
-        qraw[hh][u] = h < H ? __ldg(reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(a.q) +
-                                                                     ((long long)row * H + h) * D + lane * (D / 32)) + u)
-                            : make_uint4(0, 0, 0, 0);
-    }
-  }
+  // warp w converts heads w, w+16, ...; lane holds D/32 consecutive dims (its
+  // 16-byte query loads were issued at the top)
   __syncthreads();   // ksrc, qcs visible
   uint4 gbuf[kGatherPer];
   gather_load(gbuf);
@@ -328,22 +332,35 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttendArgs a) {
     }
     // ---- logits: warp (g, qq): heads 16g..16g+15 x keys 16qq..16qq+15
     if (16 * g < H) {
-      float sn[2][4] = {}, sr[2][4] = {};
+      // e4m3 part: two accumulator chains per n-tile (even / odd K steps) so the
+      // dependent MMAs interleave; rotary part: one chain per n-tile
+      float sn[2][4] = {}, sn2[2][4] = {}, sr[2][4] = {};
       const uint32_t qa = su32(Qs + (16 * g + (lane & 15)) * LDQ + (lane >> 4) * 8);
       const uint32_t kb = su32(Ks + (16 * qq + (lane & 7) + ((lane >> 4) << 3)) * LDQ + ((lane >> 3) & 1) * 8);
 #pragma unroll 4
-      for (int ks = 0; ks < D / 16; ++ks) {
+      for (int ks = 0; ks < DN / 16; ks += 2) {
+        uint32_t a0, a1, a2, a3, b0, b1, b2, b3, c0, c1, c2, c3, d0, d1, d2, d3;
+        ldm_x4(qa + ks * 32, a0, a1, a2, a3);
+        ldm_x4(kb + ks * 32, b0, b1, b2, b3);
+        ldm_x4(qa + ks * 32 + 32, c0, c1, c2, c3);
+        ldm_x4(kb + ks * 32 + 32, d0, d1, d2, d3);
+        mma16816(sn[0], a0, a1, a2, a3, b0, b1);
+        mma16816(sn[1], a0, a1, a2, a3, b2, b3);
+        mma16816(sn2[0], c0, c1, c2, c3, d0, d1);
+        mma16816(sn2[1], c0, c1, c2, c3, d2, d3);
+      }
+#pragma unroll
+      for (int ks = DN / 16; ks < D / 16; ++ks) {
         uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
         ldm_x4(qa + ks * 32, a0, a1, a2, a3);
         ldm_x4(kb + ks * 32, b0, b1, b2, b3);
-        if (ks < DN / 16) {
-          mma16816(sn[0], a0, a1, a2, a3, b0, b1);
-          mma16816(sn[1], a0, a1, a2, a3, b2, b3);
-        } else {
-          mma16816(sr[0], a0, a1, a2, a3, b0, b1);
-          mma16816(sr[1], a0, a1, a2, a3, b2, b3);
-        }
+        mma16816(sr[0], a0, a1, a2, a3, b0, b1);
+        mma16816(sr[1], a0, a1, a2, a3, b2, b3);
       }
+#pragma unroll
+      for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) sn[n][r] += sn2[n][r];
 #pragma unroll
       for (int n = 0; n < 2; ++n)
 #pragma unroll
@@ -486,7 +503,8 @@ cudaError_t launch_attend_tc(const AttendArgs &a, int rows, cudaStream_t st) {
   case D:                                                                                         \
     e = cudaFuncSetAttribute(k_attend_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
     if (e != cudaSuccess) return e;                                                               \
-    k_attend_tc<D><<<grid, kThreads, smem, st>>>(a);                                              \
+    e = launch_pdl(k_attend_tc<D>, grid, dim3(kThreads), smem, st, 1, a);                         \
+    if (e != cudaSuccess) return e;                                                               \
     break;
     CASE(128) CASE(256) CASE(384) CASE(512)
 #undef CASE

@@ -91,17 +91,38 @@ __device__ __forceinline__ float warp_max(float v) {
   for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
 }
+__device__ __forceinline__ int warp_sum_int(int v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
 
-// Order-preserving map float -> uint32 (larger float -> larger key).
+// Order-preserving map float -> uint32 (larger float -> larger key); -0 and +0
+// get the same key, as they compare equal.
 __device__ __forceinline__ uint32_t float_key(float f) {
-  const uint32_t u = __float_as_uint(f);
+  const uint32_t u = f == 0.f ? 0u : __float_as_uint(f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
+
+// Programmatic dependent launch (off unless built with -DCSA_PDL).  With it,
+// kernels of one step are launched with programmatic stream serialization, so a
+// kernel may start while its predecessor finishes.  pdl_wait() blocks until the
+// predecessor grid has completed and its writes are visible; every kernel calls
+// pdl_trigger() only after its own pdl_wait(), so code before pdl_wait() may read
+// anything written two or more kernels earlier, never the direct predecessor's
+// output.  Without it both are no-ops and stream order serialises the kernels.
+#ifdef CSA_PDL
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+#else
+__device__ __forceinline__ void pdl_wait() {}
+__device__ __forceinline__ void pdl_trigger() {}
+#endif
 
 // Device status word at the start of every workspace.
 struct WsHeader {

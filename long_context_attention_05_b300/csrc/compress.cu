@@ -145,6 +145,8 @@ __global__ void __launch_bounds__(1024) k_compress(CompressArgs a) {
   float *xs = smem;                 // [d + d_idx]
   float *red = smem + 1024;         // [32]
   const int b = blockIdx.y;
+  pdl_wait();      // the previous step's attention reads the ring and n_tokens
+  pdl_trigger();
   const long long n0 = a.c.n_tokens[b];
   const long long j0 = n0 / a.c.m, j1 = (n0 + a.n_new - 1) / a.c.m;
   if (blockIdx.x == 0) {
@@ -179,8 +181,7 @@ cudaError_t launch_compress(const CacheView &c, const RopeTable &rope, int batch
   const int threads = ((c.d + c.d_idx + 31) / 32) * 32;
   const int nblk = n_new == 1 ? 1 : (n_new + c.m - 1) / c.m + 1;
   const size_t smem = (1024 + 32) * sizeof(float);
-  k_compress<<<dim3(nblk, batch), threads, smem, st>>>(a);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(k_compress, dim3(nblk, batch), dim3(threads), smem, st, 1, a);
   if (e != cudaSuccess || n_new == 1) return e;
   k_advance<<<(batch + 127) / 128, 128, 0, st>>>(c.n_tokens, batch, n_new);
   return cudaGetLastError();

@@ -28,6 +28,8 @@ __global__ void __launch_bounds__(256) k_index_generic(CacheView c, int n_q, con
   float *ws = sm + heads_idx * DI;           // [heads_idx]
   const int row = blockIdx.y;                // b * n_q + i
   const int b = row / n_q, i = row % n_q;
+  pdl_wait();
+  pdl_trigger();
   const long long t = c.n_tokens[b] - n_q + i;
   const long long n_vis = min((t + 1) / c.m, c.cap);
   const long long j = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -82,8 +84,11 @@ cudaError_t launch_index_generic(const CacheView &c, int batch, int n_q, const v
   case D:                                                                                                    \
     if (smem > 48 * 1024)                                                                                    \
       cudaFuncSetAttribute(k_index_generic<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);      \
-    k_index_generic<D><<<grid, threads, smem, st>>>(c, n_q, (const uint8_t *)q_idx, q_dtype, w, heads_idx,   \
-                                                    scores, stride);                                         \
+    {                                                                                                        \
+      cudaError_t e = launch_pdl(k_index_generic<D>, grid, dim3(threads), smem, st, 1, c, n_q,               \
+                                 (const uint8_t *)q_idx, q_dtype, w, heads_idx, scores, stride);             \
+      if (e != cudaSuccess) return e;                                                                        \
+    }                                                                                                        \
     break;
     CASE(16) CASE(32) CASE(64) CASE(128)
 #undef CASE

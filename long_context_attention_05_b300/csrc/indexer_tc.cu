@@ -22,14 +22,14 @@
 // The epilogue thread of TMEM lane l owns entry l of the tile:
 //   score = s_j * sum_h (w_h / S_h) * ReLU(D_hi[h] + D_lo[h] / 16).
 //
-// Warp roles (320 threads): warp 0 = TMA producer, warp 1 = MMA issuer and TMEM
-// owner, warps 2..9 = two epilogue warpgroups that take alternate tiles (warp w
+// Warp roles (448 threads): warp 0 = TMA producer, warp 1 = MMA issuer and TMEM
+// owner, warps 2..13 = three epilogue warpgroups that take tiles in turn (warp w
 // reads TMEM lane group w % 4).  Pipelines: an 8-stage shared-memory ring of key
 // tiles (full/empty mbarriers) and up to four TMEM accumulator buffers
 // (tmem_full/tmem_empty).  Every wait is bounded; a
 // timeout sets the workspace status word and all roles stop issuing work.
-// grid = (CTAs per query row, query rows); each CTA scores a contiguous range of
-// 128-entry tiles of one row, so its query operand is built once.
+// Each CTA scores a contiguous range of 128-entry tiles of one query row, so its
+// query operand is built once (see the work assignment at the top of the kernel).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -42,8 +42,8 @@ constexpr int kTileM = 128;
 constexpr int kDI = 128;
 constexpr int kStages = 8;
 constexpr int kStageBytes = kTileM * kDI;
-constexpr int kThreads = 320;
-constexpr int kEpiGroups = 2;   // epilogue warpgroups; group e takes tiles it % 2 == e
+constexpr int kEpiGroups = 3;   // epilogue warpgroups; group e takes tiles it % 3 == e
+constexpr int kThreads = 64 + 128 * kEpiGroups;
 constexpr long long kWaitLimit = 1LL << 24;
 
 struct TcArgs {
@@ -53,7 +53,9 @@ struct TcArgs {
   const float *w;
   float *scores;
   long long stride;
-  int ctas_per_row;
+  int ctas_per_row;   // > 0: grid (ctas_per_row, rows); 0: flat grid, proportional split
+  int rows;           // query rows (batch * n_q)
+  int grid_sms;       // G of the proportional split
   int box_rows;       // rows per TMA box: 128 (contiguous) or the page size
   int *status;        // workspace status word (may be null)
 };
@@ -149,13 +151,62 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const CacheView &c = a.c;
-  const int row = blockIdx.y;
+  // ---- work assignment.  Many query rows (>= one per SM): CTA y takes row y.
+  // Few rows: the grid is flat (one CTA per SM) and row r gets
+  // max(1, floor((SMs - rows) * tiles_r / T)) CTAs (T = all rows' tiles), so ragged
+  // context lengths stay balanced; every CTA derives the same partition from n_tokens.
+  __shared__ int sh_row, sh_sub, sh_cnt;
+  pdl_wait();      // n_tokens comes from the compressor just before
+  pdl_trigger();
+  if (a.ctas_per_row > 0) {
+    if (threadIdx.x == 0) { sh_row = blockIdx.y; sh_sub = blockIdx.x; sh_cnt = a.ctas_per_row; }
+  } else if (threadIdx.x < 32) {
+    const int rows = gridDim.y == 1 ? a.rows : 0;
+    long long T = 0;
+    for (int r = threadIdx.x; r < rows; r += 32) {
+      const long long tr = min((c.n_tokens[r / a.n_q] - a.n_q + r % a.n_q + 1) / c.m, c.cap);
+      T += (tr + kTileM - 1) / kTileM;
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) T += __shfl_xor_sync(0xffffffffu, T, o);
+    int found_row = -1, found_sub = 0, found_cnt = 0;
+    long long base = 0;
+    for (int r0 = 0; r0 < rows; r0 += 32) {
+      const int r = r0 + (int)threadIdx.x;
+      long long cr = 0;
+      if (r < rows) {
+        const long long tr = (min((c.n_tokens[r / a.n_q] - a.n_q + r % a.n_q + 1) / c.m, c.cap) + kTileM - 1) / kTileM;
+        cr = tr > 0 ? max(1LL, (long long)(a.grid_sms - a.rows) * tr / max(T, 1LL)) : 0;
+      }
+      long long incl = cr;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+        if ((int)threadIdx.x >= o) incl += y;
+      }
+      const long long start = base + incl - cr;
+      const bool mine = cr > 0 && (long long)blockIdx.x >= start && (long long)blockIdx.x < start + cr;
+      const unsigned who = __ballot_sync(0xffffffffu, mine);
+      if (who) {
+        const int src = __ffs(who) - 1;
+        found_row = __shfl_sync(0xffffffffu, r, src);
+        found_sub = (int)(blockIdx.x - __shfl_sync(0xffffffffu, start, src));
+        found_cnt = (int)__shfl_sync(0xffffffffu, cr, src);
+        break;
+      }
+      base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (threadIdx.x == 0) { sh_row = found_row; sh_sub = found_sub; sh_cnt = found_cnt; }
+  }
+  __syncthreads();
+  if (sh_row < 0) return;   // uniform: a spare CTA of the flat grid
+  const int row = sh_row;
   const int b = row / a.n_q, iq = row % a.n_q;
   const long long t = c.n_tokens[b] - a.n_q + iq;
   const long long n_vis = min((t + 1) / c.m, c.cap);
   const long long n_tiles = (n_vis + kTileM - 1) / kTileM;
-  const long long tile_lo = (long long)blockIdx.x * n_tiles / a.ctas_per_row;
-  const long long tile_hi = (long long)(blockIdx.x + 1) * n_tiles / a.ctas_per_row;
+  const long long tile_lo = (long long)sh_sub * n_tiles / sh_cnt;
+  const long long tile_hi = (long long)(sh_sub + 1) * n_tiles / sh_cnt;
   if (tile_lo >= tile_hi) return;   // uniform: nothing allocated yet
   const int n_it = (int)(tile_hi - tile_lo);
   const int H = a.heads;
@@ -266,23 +317,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
     }
   } else {   // ---- epilogue: TMEM lane group g = warp % 4 owns entries 32g .. 32g+31 of a tile
     const int g = warp & 3;
-    const int grp = (warp - 2) >> 2;   // epilogue group: tiles it with it % 2 == grp
+    // Groups take tiles in turn.  A group waits on an accumulator's next phase only
+    // after finishing its previous tile, so the accumulator's previous use must be
+    // older than that tile (parity waits would alias otherwise): groups <= buffers.
+    const int n_grp = min(kEpiGroups, n_acc);
+    const int grp = (warp - 2) >> 2;   // epilogue group: tiles it with it % n_grp == grp
     // key scales are read four of this group's tiles ahead so their memory
     // latency overlaps the tiles in between instead of stalling each epilogue
     auto scale_of = [&](int it2) -> float {
       const long long j2 = (tile_lo + it2) * kTileM + g * 32 + lane;
       return (it2 < n_it && j2 < n_vis) ? __ldg(c.idx_scale + entry_row(c, b, j2)) : 0.f;
     };
-    // slot u of sc[] holds the scale of this group's tile it0 + 2u; it is refilled
+    // slot u of sc[] holds the scale of this group's tile it0 + n_grp*u; it is refilled
     // in place four tiles ahead (no register shuffling that would wait on loads)
     float sc[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) sc[u] = scale_of(grp + 2 * u);
+    for (int u = 0; u < 4; ++u) sc[u] = scale_of(grp + n_grp * u);
     bool live = true;
-    for (int it0 = grp; it0 < n_it && live; it0 += 4 * kEpiGroups) {
+    if (grp >= n_grp) live = false;
+    for (int it0 = grp; it0 < n_it && live; it0 += 4 * n_grp) {
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int it = it0 + kEpiGroups * u;
+        const int it = it0 + n_grp * u;
         if (it >= n_it || !live) break;
         const int acc = it % n_acc;
         const uint32_t aph = (uint32_t)(it / n_acc) & 1u;
@@ -307,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
         const float sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
         const long long j = (tile_lo + it) * kTileM + g * 32 + lane;
         if (j < n_vis) a.scores[(long long)row * a.stride + j] = sum * sc[u];
-        sc[u] = scale_of(it + 4 * kEpiGroups);
+        sc[u] = scale_of(it + 4 * n_grp);
       }
     }
   }
@@ -370,16 +426,20 @@ cudaError_t launch_index_tc(const CacheView &c, int batch, int n_q, const void *
   a.q_idx = (const uint8_t *)q_idx; a.w = w; a.scores = scores; a.stride = stride;
   a.box_rows = box_rows; a.status = status;
   const int rows_q = batch * n_q;
-  const long long max_tiles = (c.cap + kTileM - 1) / kTileM;
-  long long cpr = (num_sms + rows_q - 1) / rows_q;
-  if (cpr > max_tiles) cpr = max_tiles;
-  if (cpr < 1) cpr = 1;
-  a.ctas_per_row = (int)cpr;
+  a.rows = rows_q;
+  a.grid_sms = num_sms;
+  dim3 grid;
+  if (rows_q >= num_sms) {   // a row per CTA
+    a.ctas_per_row = 1;
+    grid = dim3(1, rows_q);
+  } else {                   // flat grid, CTAs split over rows by their tile counts: at most
+    a.ctas_per_row = 0;       // (SMs - rows) * share + 1 per row, i.e. <= SMs in all
+    grid = dim3(num_sms, 1);
+  }
   const size_t smem = index_tc_smem_bytes();
   cudaError_t e = cudaFuncSetAttribute(k_index_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  k_index_tc<<<dim3((unsigned)cpr, rows_q), kThreads, smem, st>>>(map, a);
-  return cudaGetLastError();
+  return launch_pdl(k_index_tc, grid, dim3(kThreads), smem, st, 1, map, a);
 }
 
 }  // namespace csa

@@ -52,6 +52,8 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_row(CacheView c, int n_q,
   __shared__ int sh_krem;
   const int row = blockIdx.x;
   const int b = row / n_q, i = row % n_q;
+  pdl_wait();
+  pdl_trigger();
   const long long t = c.n_tokens[b] - n_q + i;
   long long n = min((t + 1) / c.m, c.cap);
   if (n > stride) n = stride;
@@ -120,34 +122,53 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_row(CacheView c, int n_q,
   if (threadIdx.x == 0) out_count[row] = k;
 }
 
-// Cluster version: the CS CTAs of one thread-block cluster share a query row.
-// Each CTA keeps its slice of the row's keys in shared memory.  Three radix
-// passes (11, 11 and 10 bits): each CTA builds the digit histogram of its
-// slice; the cluster reduces it (CTA r sums bins of its own range over all
-// peers) and gathers the merged histogram back through distributed shared
-// memory, so every CTA holds the same histogram and reaches the same digit.
-// Histograms are double-buffered across passes, so a pass costs two cluster
-// barriers.  The compaction writes in index order: a CTA's output offset is
-// what its lower-ranked peers select; within a CTA each thread owns a
-// contiguous run of keys and one block scan orders them.
+// Cluster version: the CS CTAs of one thread-block cluster share a query row;
+// each keeps its slice of the row's keys in shared memory.
+//   1. cluster-wide min and max of the scores;
+//   2. one histogram over 2048 equal-width VALUE bins of [min, max] (monotone:
+//      a key in a higher bin is larger than every key in a lower one), merged
+//      across the cluster through distributed shared memory (CTA r sums its own
+//      bin range over all peers, then every CTA gathers the merged counts);
+//   3. the bin holding the k-th largest score is found by a scan from the top;
+//      the few keys of that bin are gathered from all peers and the exact k-th
+//      key T is found among them by rank counting;
+//   4. compaction in index order: keys > T, then keys == T lowest index first.
+// Bins that are too crowded (degenerate value ranges) fall back to three radix
+// passes over the ordered-integer keys.  Every decision is integer counting on
+// identical data in every CTA, so the result is deterministic.
 constexpr int kBins = 2048;
+constexpr int kCandMax = 2048;
+
+__device__ __forceinline__ float key_float(unsigned key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
 
 __global__ void __launch_bounds__(kTopkThreads) k_topk_cluster(CacheView c, int n_q, const float *scores,
                                                                long long stride, int k, int32_t *out_idx,
                                                                int32_t *out_count, int slice_cap) {
   namespace cg = cooperative_groups;
   cg::cluster_group cl = cg::this_cluster();
-  extern __shared__ unsigned keys[];             // [slice_cap]
-  __shared__ unsigned hist[2][kBins];            // this CTA's slice histogram (double-buffered)
-  __shared__ unsigned part[2][kBins];            // merged counts of this CTA's bin range
+  extern __shared__ unsigned keys[];             // [slice_cap] keys, then [slice_cap] uint16 bins
+  unsigned short *kbin = reinterpret_cast<unsigned short *>(keys + slice_cap);
+  __shared__ unsigned hist[4][kBins];            // this CTA's slice histogram, four sub-copies
+  __shared__ unsigned part[kBins];               // merged counts of this CTA's bin range
+  __shared__ unsigned cand[kCandMax];            // rank 0: every CTA's candidates; then a private copy
+  __shared__ unsigned char cand_rank[kCandMax];  // ... and the rank each came from
+  __shared__ int above_r[16];                    // rank 0: each CTA's count of keys above the bin
+  __shared__ int gt_r[16], eq_r[16];             // per rank: keys > T, keys == T
   __shared__ int scan_buf[64];
+  __shared__ unsigned red_u[64];
+  __shared__ unsigned sh_minmax[2];              // this CTA's (min, max) key
+  __shared__ int sh_cand;                        // rank 0: candidates appended so far
   __shared__ unsigned sh_prefix;
-  __shared__ int sh_krem;
+  __shared__ int sh_krem, sh_bin, sh_above, sh_incount;
   __shared__ int cnt[2];                         // this CTA's (greater, equal) counts
   const int CS = (int)cl.num_blocks();
   const int rank = (int)cl.block_rank();
   const int row = blockIdx.y;
   const int b = row / n_q, i = row % n_q;
+  pdl_wait();
+  pdl_trigger();
   const long long t = c.n_tokens[b] - n_q + i;
   long long n = min((t + 1) / c.m, c.cap);
   if (n > stride) n = stride;
@@ -159,78 +180,266 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_cluster(CacheView c, int 
     }
     return;
   }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = (int)blockDim.x >> 5;
   const long long L = (n + CS - 1) / CS;
   const long long lo = min(n, rank * L), hi = min(n, lo + L);
   const int len = (int)(hi - lo);
   const float *s = scores + (long long)row * stride + lo;
-  // eight loads in flight per thread per round (not one memory round trip per key)
-  for (int j0 = 0; j0 < len; j0 += 8 * kTopkThreads) {
-    float v[8];
+  // ---- load: 16-byte loads for the aligned middle, scalars for the ends; and the
+  //      slice's min / max key
+  unsigned kmin = 0xFFFFFFFFu, kmax = 0u;
+  {
+    const int head = min(len, (int)((4 - (((uintptr_t)s >> 2) & 3)) & 3));
+    const int nvec = (len - head) >> 2;
+    const float4 *sv = reinterpret_cast<const float4 *>(s + head);
+    for (int v0 = 0; v0 < nvec; v0 += 4 * kTopkThreads) {
+      float4 v[4];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int j = j0 + q * kTopkThreads + (int)threadIdx.x;
-      v[q] = j < len ? __ldg(s + j) : 0.f;
-    }
+      for (int q = 0; q < 4; ++q) {
+        const int x = v0 + q * kTopkThreads + (int)threadIdx.x;
+        v[q] = x < nvec ? __ldg(sv + x) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int j = j0 + q * kTopkThreads + (int)threadIdx.x;
-      if (j < len) keys[j] = float_key(v[q]);
-    }
-  }
-  const int per = kBins / CS;                    // bins this CTA reduces
-  unsigned prefix = 0, mask = 0;
-  int krem = k;
-  const int shifts[3] = {21, 10, 0};
-  const int widths[3] = {11, 11, 10};
-  for (int pass = 0; pass < 3; ++pass) {
-    const int shift = shifts[pass];
-    const unsigned dmask = (1u << widths[pass]) - 1u;
-    unsigned *h = hist[pass & 1];
-    unsigned *pm = part[pass & 1];
-    for (int e = threadIdx.x; e < kBins; e += blockDim.x) h[e] = 0;
-    __syncthreads();
-    for (int j = threadIdx.x; j < len; j += blockDim.x) {
-      const unsigned key = keys[j];
-      const bool in = (key & mask) == prefix;
-      const unsigned bin = (key >> shift) & dmask;
-      const unsigned act = __ballot_sync(__activemask(), in);
-      if (in) {
-        const unsigned peers = __match_any_sync(act, bin);
-        if ((threadIdx.x & 31) == (unsigned)(__ffs(peers) - 1)) atomicAdd(&h[bin], __popc(peers));
+      for (int q = 0; q < 4; ++q) {
+        const int x = v0 + q * kTopkThreads + (int)threadIdx.x;
+        if (x < nvec) {
+          const unsigned k0 = float_key(v[q].x), k1 = float_key(v[q].y), k2 = float_key(v[q].z), k3 = float_key(v[q].w);
+          unsigned *kd = keys + head + 4 * x;   // not 16-byte aligned in general: scalar stores
+          kd[0] = k0; kd[1] = k1; kd[2] = k2; kd[3] = k3;
+          kmin = min(min(kmin, min(k0, k1)), min(k2, k3));
+          kmax = max(max(kmax, max(k0, k1)), max(k2, k3));
+        }
       }
     }
-    cl.sync();   // all slice histograms complete
-    for (int e = threadIdx.x; e < per; e += blockDim.x) {
-      unsigned v[16];
-#pragma unroll
-      for (int r = 0; r < 16; ++r) v[r] = r < CS ? cl.map_shared_rank(h, r)[rank * per + e] : 0u;   // all in flight
-      unsigned sum = 0;
-#pragma unroll
-      for (int r = 0; r < 16; ++r) sum += v[r];
-      pm[rank * per + e] = sum;
+    for (int j = threadIdx.x; j < len; j += blockDim.x) {   // the unaligned ends
+      if (j < head || j >= head + 4 * nvec) {
+        const unsigned key = float_key(__ldg(s + j));
+        keys[j] = key;
+        kmin = min(kmin, key);
+        kmax = max(kmax, key);
+      }
     }
-    cl.sync();   // every CTA's merged range complete
-    // gather the merged histogram; thread x owns bins 2047-2x and 2046-2x (descending)
-    const int b0 = kBins - 1 - 2 * (int)threadIdx.x, b1 = b0 - 1;
-    const unsigned c0 = cl.map_shared_rank(pm, b0 / per)[b0];
-    const unsigned c1 = cl.map_shared_rank(pm, b1 / per)[b1];
-    int tot;
-    const int above = block_exclusive_scan((int)(c0 + c1), scan_buf, tot);   // keys in higher bins
-    if (above < krem && above + (int)(c0 + c1) >= krem) {
-      const bool first = above + (int)c0 >= krem;
-      sh_prefix = prefix | ((unsigned)(first ? b0 : b1) << shift);
-      sh_krem = krem - (first ? above : above + (int)c0);
+  }
+  kmin = __reduce_min_sync(0xffffffffu, kmin);
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  if (lane == 0) { red_u[warp] = kmin; red_u[32 + warp] = kmax; }
+  for (int e = threadIdx.x; e < kBins; e += blockDim.x) {
+    hist[0][e] = 0; hist[1][e] = 0; hist[2][e] = 0; hist[3][e] = 0;
+    part[e] = 0;
+  }
+  if (threadIdx.x < 16) { gt_r[threadIdx.x] = 0; eq_r[threadIdx.x] = 0; }
+  if (threadIdx.x == 0) sh_cand = 0;
+  __syncthreads();
+  if (warp == 0) {
+    unsigned a = lane < nwarps ? red_u[lane] : 0xFFFFFFFFu, z = lane < nwarps ? red_u[32 + lane] : 0u;
+    a = __reduce_min_sync(0xffffffffu, a);
+    z = __reduce_max_sync(0xffffffffu, z);
+    if (lane == 0) { sh_minmax[0] = a; sh_minmax[1] = z; }
+  }
+  cl.sync();   // S1: every CTA's (min, max) visible; every part[] / counter zeroed
+  unsigned gmin = 0xFFFFFFFFu, gmax = 0u;
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    if (r < CS) {
+      const unsigned *mm = cl.map_shared_rank(sh_minmax, r);
+      gmin = min(gmin, mm[0]);
+      gmax = max(gmax, mm[1]);
+    }
+  }
+  const float vmin = key_float(gmin), vmax = key_float(gmax);
+  const float scale = (float)kBins / (vmax - vmin);
+  const bool binned = gmax > gmin && isfinite(scale) && scale > 0.f && isfinite(vmin) && isfinite(vmax);
+  unsigned prefix = 0;
+  int krem = k;
+  bool need_radix = !binned;
+  bool fast_offsets = false;   // output offsets known from rank 0's lists (no count exchange)
+  if (binned) {
+    // ---- value histogram (bin(v) is monotone in v); non-empty bins are added
+    //      straight into the owner CTA's merged array
+    const int per = kBins / CS;
+    unsigned *hsub = hist[warp & 3];
+    for (int j = threadIdx.x; j < len; j += blockDim.x) {
+      const int bin = min(kBins - 1, (int)((key_float(keys[j]) - vmin) * scale));
+      kbin[j] = (unsigned short)bin;
+      atomicAdd(&hsub[bin], 1u);
     }
     __syncthreads();
-    prefix = sh_prefix;
-    krem = sh_krem;
-    mask |= dmask << shift;
+    for (int e = threadIdx.x; e < kBins; e += blockDim.x) {
+      const unsigned v = hist[0][e] + hist[1][e] + hist[2][e] + hist[3][e];
+      hist[0][e] = v;
+      if (v) atomicAdd(cl.map_shared_rank(part, e / per) + e, v);
+    }
+    cl.sync();   // S2: merged histogram complete
+    // thread x owns bins 2047-2x and 2046-2x (descending)
+    const int b0 = kBins - 1 - 2 * (int)threadIdx.x, b1 = b0 - 1;
+    const unsigned c0 = cl.map_shared_rank(part, b0 / per)[b0];
+    const unsigned c1 = cl.map_shared_rank(part, b1 / per)[b1];
+    int tot;
+    const int above = block_exclusive_scan((int)(c0 + c1), scan_buf, tot);   // keys in higher bins
+    if (above < k && above + (int)(c0 + c1) >= k) {
+      const bool first = above + (int)c0 >= k;
+      sh_bin = first ? b0 : b1;
+      sh_above = first ? above : above + (int)c0;
+      sh_incount = (int)(first ? c0 : c1);
+    }
+    __syncthreads();
+    const int bstar = sh_bin, kin = k - sh_above, total = sh_incount;
+    if (total <= kCandMax) {
+      // ---- the threshold bin's keys of every CTA (with their rank) and every CTA's
+      //      count of keys above the bin go to rank 0
+      unsigned *cand0 = cl.map_shared_rank(cand, 0);
+      unsigned char *crank0 = cl.map_shared_rank(cand_rank, 0);
+      int *cnt0 = cl.map_shared_rank(&sh_cand, 0);
+      for (int j = threadIdx.x; j < len; j += blockDim.x)
+        if (kbin[j] == bstar) {
+          const int slot = atomicAdd(cnt0, 1);
+          cand0[slot] = keys[j];
+          crank0[slot] = (unsigned char)rank;
+        }
+      {
+        int ab = 0;   // keys of this slice in bins above b*
+        for (int e = bstar + 1 + (int)threadIdx.x; e < kBins; e += blockDim.x) ab += (int)hist[0][e];
+        ab = warp_sum_int(ab);
+        if (lane == 0) scan_buf[warp] = ab;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+          int sum = 0;
+          for (int w = 0; w < nwarps; ++w) sum += scan_buf[w];
+          cl.map_shared_rank(above_r, 0)[rank] = sum;
+        }
+      }
+      cl.sync();   // S3: rank 0 holds all `total` candidates and every CTA's count above
+      unsigned mine[2] = {0u, 0u};
+      unsigned char mrank[2] = {0, 0};
+#pragma unroll
+      for (int slot = 0; slot < 2; ++slot) {
+        const int x = (int)threadIdx.x + slot * (int)blockDim.x;
+        if (x < total) { mine[slot] = cand0[x]; mrank[slot] = crank0[x]; }
+      }
+      int ab_r = 0;
+      if (threadIdx.x < 16 && (int)threadIdx.x < CS) ab_r = cl.map_shared_rank(above_r, 0)[threadIdx.x];
+      cl.barrier_arrive();   // done reading rank 0; the matching wait is at the very end
+      fast_offsets = true;
+      __syncthreads();
+#pragma unroll
+      for (int slot = 0; slot < 2; ++slot) {
+        const int x = (int)threadIdx.x + slot * (int)blockDim.x;
+        if (x < total) { cand[x] = mine[slot]; cand_rank[x] = mrank[slot]; }
+      }
+      if (threadIdx.x < 16) gt_r[threadIdx.x] = ab_r;
+      __syncthreads();
+      if (total <= 128) {
+        // exact rank of each candidate among the candidates
+        if ((int)threadIdx.x < total) {
+          const unsigned key = cand[threadIdx.x];
+          int gtc = 0, eqc = 0;
+          for (int y = 0; y < total; ++y) {
+            gtc += cand[y] > key;
+            eqc += cand[y] == key;
+          }
+          if (gtc < kin && gtc + eqc >= kin) {   // several equal keys write the same values
+            sh_prefix = key;
+            sh_krem = kin - gtc;
+          }
+        }
+        __syncthreads();
+        prefix = sh_prefix;
+        krem = sh_krem;
+      } else {
+        // three radix passes over the candidates, inside this CTA (no cluster barrier)
+        unsigned pre = 0, msk = 0;
+        int kr = kin;
+        const int shifts[3] = {21, 10, 0};
+        const int widths[3] = {11, 11, 10};
+        for (int pass = 0; pass < 3; ++pass) {
+          const int shift = shifts[pass];
+          const unsigned dmask = (1u << widths[pass]) - 1u;
+          for (int e = threadIdx.x; e < kBins; e += blockDim.x) hist[0][e] = 0;
+          __syncthreads();
+          for (int x = threadIdx.x; x < total; x += blockDim.x) {
+            const unsigned key = cand[x];
+            if ((key & msk) == pre) atomicAdd(&hist[0][(key >> shift) & dmask], 1u);
+          }
+          __syncthreads();
+          const int b0 = kBins - 1 - 2 * (int)threadIdx.x, b1 = b0 - 1;
+          const unsigned c0 = hist[0][b0], c1 = hist[0][b1];
+          int tot2;
+          const int above2 = block_exclusive_scan((int)(c0 + c1), scan_buf, tot2);
+          if (above2 < kr && above2 + (int)(c0 + c1) >= kr) {
+            const bool first = above2 + (int)c0 >= kr;
+            sh_prefix = pre | ((unsigned)(first ? b0 : b1) << shift);
+            sh_krem = kr - (first ? above2 : above2 + (int)c0);
+          }
+          __syncthreads();
+          pre = sh_prefix;
+          kr = sh_krem;
+          msk |= dmask << shift;
+        }
+        prefix = pre;
+        krem = kr;
+      }
+      // per rank: keys > T (above the bin, or candidates above T) and keys == T
+      for (int x = threadIdx.x; x < total; x += blockDim.x) {
+        if (cand[x] > prefix) atomicAdd(&gt_r[cand_rank[x]], 1);
+        else if (cand[x] == prefix) atomicAdd(&eq_r[cand_rank[x]], 1);
+      }
+      __syncthreads();
+    } else {
+      need_radix = true;
+    }
+  }
+  if (need_radix) {
+    // ---- fallback: three radix passes (11, 11, 10 bits) on the ordered keys
+    unsigned mask = 0;
+    const int shifts[3] = {21, 10, 0};
+    const int widths[3] = {11, 11, 10};
+    const int per = kBins / CS;
+    for (int pass = 0; pass < 3; ++pass) {
+      const int shift = shifts[pass];
+      const unsigned dmask = (1u << widths[pass]) - 1u;
+      for (int e = threadIdx.x; e < kBins; e += blockDim.x) hist[0][e] = 0;
+      cl.sync();   // peers are done reading the previous histogram
+      for (int j = threadIdx.x; j < len; j += blockDim.x) {
+        const unsigned key = keys[j];
+        const bool in = (key & mask) == prefix;
+        const unsigned bin = (key >> shift) & dmask;
+        const unsigned act = __ballot_sync(__activemask(), in);
+        if (in) {
+          const unsigned peers = __match_any_sync(act, bin);
+          if ((threadIdx.x & 31) == (unsigned)(__ffs(peers) - 1)) atomicAdd(&hist[0][bin], __popc(peers));
+        }
+      }
+      cl.sync();
+      for (int e = threadIdx.x; e < per; e += blockDim.x) {
+        unsigned v[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) v[r] = r < CS ? cl.map_shared_rank(&hist[0][0], r)[rank * per + e] : 0u;
+        unsigned sum = 0;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) sum += v[r];
+        part[rank * per + e] = sum;
+      }
+      cl.sync();
+      const int b0 = kBins - 1 - 2 * (int)threadIdx.x, b1 = b0 - 1;
+      const unsigned c0 = cl.map_shared_rank(part, b0 / per)[b0];
+      const unsigned c1 = cl.map_shared_rank(part, b1 / per)[b1];
+      int tot;
+      const int above = block_exclusive_scan((int)(c0 + c1), scan_buf, tot);
+      if (above < krem && above + (int)(c0 + c1) >= krem) {
+        const bool first = above + (int)c0 >= krem;
+        sh_prefix = prefix | ((unsigned)(first ? b0 : b1) << shift);
+        sh_krem = krem - (first ? above : above + (int)c0);
+      }
+      cl.sync();   // digit published; peers done reading part
+      prefix = sh_prefix;
+      krem = sh_krem;
+      mask |= dmask << shift;
+    }
   }
   // prefix = T, the k-th largest key; krem keys equal to T are still to be taken.
   // Warp w owns the contiguous run [w*seg, (w+1)*seg) of this slice and walks it
   // 32 keys at a time (coalesced, conflict-free); ballots order keys inside a
   // round, one block scan orders the warps.
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = (int)blockDim.x >> 5;
   const unsigned lt = (1u << lane) - 1u;
   const int seg = ((len + nwarps - 1) / nwarps + 31) & ~31;
   const int w0 = min(len, warp * seg), w1 = min(len, w0 + seg);
@@ -244,16 +453,25 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_cluster(CacheView c, int 
   int tot;
   const int ex = block_exclusive_scan(lane == 0 ? ((ew << 16) | gw) : 0, scan_buf, tot);   // counts < 2^16
   const int wex = __shfl_sync(0xffffffffu, ex, 0);
-  if (threadIdx.x == 0) { cnt[0] = tot & 0xFFFF; cnt[1] = tot >> 16; }
-  cl.sync();
+  int pg[16], pe[16];
+  if (fast_offsets) {
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      pg[r] = r < rank ? gt_r[r] : 0;
+      pe[r] = r < rank ? eq_r[r] : 0;
+    }
+  } else {
+    if (threadIdx.x == 0) { cnt[0] = tot & 0xFFFF; cnt[1] = tot >> 16; }
+    cl.sync();
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      pg[r] = r < rank ? cl.map_shared_rank(cnt, r)[0] : 0;
+      pe[r] = r < rank ? cl.map_shared_rank(cnt, r)[1] : 0;
+    }
+    cl.barrier_arrive();
+  }
   long long base = 0;
   int eq_before = 0;
-  int pg[16], pe[16];
-#pragma unroll
-  for (int r = 0; r < 16; ++r) {
-    pg[r] = r < rank ? cl.map_shared_rank(cnt, r)[0] : 0;
-    pe[r] = r < rank ? cl.map_shared_rank(cnt, r)[1] : 0;
-  }
 #pragma unroll
   for (int r = 0; r < 16; ++r) {
     base += pg[r] + max(0, min(pe[r], krem - eq_before));
@@ -274,7 +492,7 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_cluster(CacheView c, int 
     e_seen += __popc(be);
   }
   if (rank == 0 && threadIdx.x == 0) out_count[row] = k;
-  cl.sync();   // no CTA leaves while a peer may still read its shared memory
+  cl.barrier_wait();   // no CTA leaves while a peer may still read its shared memory
 }
 
 // Rows with few queries get a cluster of up to 16 CTAs each; many rows get one
@@ -289,36 +507,24 @@ cudaError_t launch_topk(const CacheView &c, int batch, int n_q, const float *sco
     while (cs > 1 && (long long)rows * cs > 2LL * num_sms && (n_cap + cs / 2 - 1) / (cs / 2) <= 32768) cs /= 2;
   }
   const long long slice = (n_cap + cs - 1) / cs;
-  const size_t smem = (size_t)slice * sizeof(unsigned);
-  if (smem > 160 * 1024 || cs > 16 || kBins % cs) {
-    k_topk_row<<<rows, kTopkThreads, 0, st>>>(c, n_q, scores, stride, k, out_idx, out_count);
-    return cudaGetLastError();
-  }
-  cudaError_t e = cudaFuncSetAttribute(k_topk_cluster, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const size_t smem = (size_t)slice * 6;   // uint32 key + uint16 bin per score
+  if (smem > 160 * 1024 || cs > 16 || kBins % cs)
+    return launch_pdl(k_topk_row, dim3(rows), dim3(kTopkThreads), 0, st, 1, c, n_q, scores, stride, k, out_idx,
+                      out_count);
+  cudaError_t e = cudaFuncSetAttribute(k_topk_cluster, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
   if (e == cudaSuccess && cs > 8)
     e = cudaFuncSetAttribute(k_topk_cluster, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
   for (;; cs /= 2) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(cs, rows);
-    cfg.blockDim = dim3(kTopkThreads);
-    cfg.dynamicSmemBytes = (size_t)((n_cap + cs - 1) / cs) * sizeof(unsigned);
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = cs;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cfg.dynamicSmemBytes > 160 * 1024) break;
-    e = cudaLaunchKernelEx(&cfg, k_topk_cluster, c, n_q, scores, stride, k, out_idx, out_count,
-                           (int)((n_cap + cs - 1) / cs));
+    const size_t sm = (size_t)((n_cap + cs - 1) / cs) * 6;
+    if (sm > 160 * 1024) break;
+    e = launch_pdl(k_topk_cluster, dim3(cs, rows), dim3(kTopkThreads), sm, st, cs, c, n_q, scores, stride, k, out_idx,
+                   out_count, (int)((n_cap + cs - 1) / cs));
     if (e == cudaSuccess || cs == 1) return e;
     cudaGetLastError();   // cluster too large for this device: halve it
   }
-  k_topk_row<<<rows, kTopkThreads, 0, st>>>(c, n_q, scores, stride, k, out_idx, out_count);
-  return cudaGetLastError();
+  return launch_pdl(k_topk_row, dim3(rows), dim3(kTopkThreads), 0, st, 1, c, n_q, scores, stride, k, out_idx,
+                    out_count);
 }
 
 }  // namespace csa
