@@ -352,10 +352,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
           tmem_ld32(taddr + c0, hv);
           tmem_ld32(taddr + H + c0, lv);
           tmem_wait_ld();
+          // w_h/S_h as 16-byte shared loads: a quarter of the shared-memory wavefronts of
+          // scalar loads (shared-memory bandwidth is shared with the TMA writes and MMA reads)
+          const float4 *wq4 = reinterpret_cast<const float4 *>(wq + c0);
 #pragma unroll
-          for (int h = 0; h < 32; ++h)
-            s4[h & 3] = fmaf(wq[c0 + h], fmaxf(fmaf(__uint_as_float(lv[h]), 0.0625f, __uint_as_float(hv[h])), 0.f),
-                             s4[h & 3]);
+          for (int h4 = 0; h4 < 8; ++h4) {
+            const float4 wv = wq4[h4];
+            const float wk[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int h = 4 * h4 + e;
+              s4[e] = fmaf(wk[e], fmaxf(fmaf(__uint_as_float(lv[h]), 0.0625f, __uint_as_float(hv[h])), 0.f), s4[e]);
+            }
+          }
         }
         tc_fence_before();
         __syncwarp();
