@@ -155,6 +155,21 @@ def profiled_traffic():
     return traffic if sha == indexer_source_sha1() else None
 
 
+def max_over_ranks(values, device=None):
+    """Element-wise maximum of per-rank timings over all ranks (the slowest rank sets
+    the whole job's time).  Timing only: no data of the attention path is exchanged."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def job_throughput(world, queries_per_rank_step, steps, seconds):
+    """Whole-job queries/s: every rank runs its own replica batch (weak scaling)."""
+    return world * queries_per_rank_step * steps / seconds
+
+
 def _workload(name, steps_total):
     from long_context_attention_05_b300 import synthetic as S
     extra = steps_total // 4 + 16
@@ -403,14 +418,11 @@ def run_ours(args, rank, world, local_rank):
     barrier()
 
     if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([ms, e2e_s], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms, e2e_s = float(tt[0]), float(tt[1])
+        ms, e2e_s = max_over_ranks([ms, e2e_s], dev)
     w0l = layers[0]["w"]
     queries_per_step = w0l.batch * w0l.n_new
-    value = world * queries_per_step * args.steps / (ms / 1000.0)
-    e2e = world * queries_per_step * args.steps / e2e_s
+    value = job_throughput(world, queries_per_step, args.steps, ms / 1000.0)
+    e2e = job_throughput(world, queries_per_step, args.steps, e2e_s)
     hbm_peak, bf16_peak, peak_kind = _peaks()
     idx_bytes, step_bytes = _alg_bytes(w0l)
     step_bytes_all = sum(_alg_bytes(ly["w"])[1] for ly in layers)

@@ -45,6 +45,7 @@ constexpr int kStageBytes = kTileM * kDI;
 constexpr int kEpiGroups = 3;   // epilogue warpgroups; group e takes tiles it % 3 == e
 constexpr int kThreads = 64 + 128 * kEpiGroups;
 constexpr long long kWaitLimit = 1LL << 24;
+constexpr int kMaxFlatRows = 256;   // the flat grid serves fewer query rows than this
 
 struct TcArgs {
   CacheView c;
@@ -58,6 +59,7 @@ struct TcArgs {
   int grid_sms;       // G of the proportional split
   int box_rows;       // rows per TMA box: 128 (contiguous) or the page size
   int *status;        // workspace status word (may be null)
+  int q_vec;          // q_idx is 16-byte aligned: vector loads of the query
 };
 
 __device__ __forceinline__ uint32_t su32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -93,11 +95,20 @@ __device__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_fl
   return false;
 }
 
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y) {
+// Key tiles are read once per call: they go through L2 with the evict-first policy,
+// so the stream does not push out what the next kernels reuse (scores, queries,
+// window, code).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y,
+                                            uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
-          su32(dst)),
-      "l"((uint64_t)map), "r"(su32(bar)), "r"(x), "r"(y)
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(su32(dst)),
+      "l"((uint64_t)map), "r"(su32(bar)), "r"(x), "r"(y), "l"(policy)
       : "memory");
 }
 
@@ -156,86 +167,147 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
   // max(1, floor((SMs - rows) * tiles_r / T)) CTAs (T = all rows' tiles), so ragged
   // context lengths stay balanced; every CTA derives the same partition from n_tokens.
   __shared__ int sh_row, sh_sub, sh_cnt;
+  __shared__ long long sh_nvis;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_wait();      // n_tokens comes from the compressor just before
   pdl_trigger();
+  if (threadIdx.x == 32) {   // barriers (warp 1) while warp 0 works out the partition
+    for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    for (int s = 0; s < 4; ++s) { mbar_init(&tfull[s], 1); mbar_init(&tempty[s], 4); }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  auto visible = [&](long long n_tok, int r) {   // entries query row r sees
+    return min((n_tok - a.n_q + r % a.n_q + 1) / c.m, c.cap);
+  };
   if (a.ctas_per_row > 0) {
-    if (threadIdx.x == 0) { sh_row = blockIdx.y; sh_sub = blockIdx.x; sh_cnt = a.ctas_per_row; }
-  } else if (threadIdx.x < 32) {
+    if (threadIdx.x == 0) {
+      sh_row = blockIdx.y; sh_sub = blockIdx.x; sh_cnt = a.ctas_per_row;
+      sh_nvis = visible(c.n_tokens[blockIdx.y / a.n_q], blockIdx.y);
+    }
+  } else if (warp == 0) {
+    // lane l holds rows l, l+32, ...: every n_tokens load is issued before the first
+    // is used (one memory round trip); the rest is a few 32-bit shuffles per chunk of
+    // 32 rows (this runs on one warp at the start of every CTA, so it is kept short)
     const int rows = gridDim.y == 1 ? a.rows : 0;
+    const int n_chunks = (rows + 31) >> 5;
+    long long nt[kMaxFlatRows / 32];
+#pragma unroll
+    for (int u = 0; u < kMaxFlatRows / 32; ++u) {
+      const int r = lane + 32 * u;
+      nt[u] = r < rows ? c.n_tokens[r / a.n_q] : 0;
+    }
+    long long nv[kMaxFlatRows / 32];
+    int tiles[kMaxFlatRows / 32];
     long long T = 0;
-    for (int r = threadIdx.x; r < rows; r += 32) {
-      const long long tr = min((c.n_tokens[r / a.n_q] - a.n_q + r % a.n_q + 1) / c.m, c.cap);
-      T += (tr + kTileM - 1) / kTileM;
+#pragma unroll
+    for (int u = 0; u < kMaxFlatRows / 32; ++u) {
+      if (u >= n_chunks) break;   // warp-uniform
+      const int r = lane + 32 * u;
+      nv[u] = r < rows ? visible(nt[u], r) : 0;
+      tiles[u] = nv[u] > 0 ? (int)((nv[u] + kTileM - 1) / kTileM) : 0;
+      T += tiles[u];
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) T += __shfl_xor_sync(0xffffffffu, T, o);
-    int found_row = -1, found_sub = 0, found_cnt = 0;
-    long long base = 0;
-    for (int r0 = 0; r0 < rows; r0 += 32) {
-      const int r = r0 + (int)threadIdx.x;
-      long long cr = 0;
-      if (r < rows) {
-        const long long tr = (min((c.n_tokens[r / a.n_q] - a.n_q + r % a.n_q + 1) / c.m, c.cap) + kTileM - 1) / kTileM;
-        cr = tr > 0 ? max(1LL, (long long)(a.grid_sms - a.rows) * tr / max(T, 1LL)) : 0;
-      }
-      long long incl = cr;
+    int found_row = -1, found_sub = 0, found_cnt = 0, base = 0;
+    long long found_nv = 0;
+#pragma unroll
+    for (int u = 0; u < kMaxFlatRows / 32; ++u) {
+      if (u >= n_chunks) break;   // warp-uniform
+      const int r = lane + 32 * u;
+      const int cr = tiles[u] > 0 ? max(1, (int)((long long)(a.grid_sms - a.rows) * tiles[u] / max(T, 1LL))) : 0;
+      int incl = cr;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const long long y = __shfl_up_sync(0xffffffffu, incl, o);
-        if ((int)threadIdx.x >= o) incl += y;
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
       }
-      const long long start = base + incl - cr;
-      const bool mine = cr > 0 && (long long)blockIdx.x >= start && (long long)blockIdx.x < start + cr;
+      const int start = base + incl - cr;
+      const bool mine = cr > 0 && (int)blockIdx.x >= start && (int)blockIdx.x < start + cr;
       const unsigned who = __ballot_sync(0xffffffffu, mine);
-      if (who) {
+      if (who && found_row < 0) {
         const int src = __ffs(who) - 1;
         found_row = __shfl_sync(0xffffffffu, r, src);
-        found_sub = (int)(blockIdx.x - __shfl_sync(0xffffffffu, start, src));
-        found_cnt = (int)__shfl_sync(0xffffffffu, cr, src);
-        break;
+        found_sub = (int)blockIdx.x - __shfl_sync(0xffffffffu, start, src);
+        found_cnt = __shfl_sync(0xffffffffu, cr, src);
+        found_nv = __shfl_sync(0xffffffffu, nv[u], src);
       }
       base += __shfl_sync(0xffffffffu, incl, 31);
     }
-    if (threadIdx.x == 0) { sh_row = found_row; sh_sub = found_sub; sh_cnt = found_cnt; }
+    if (lane == 0) { sh_row = found_row; sh_sub = found_sub; sh_cnt = found_cnt; sh_nvis = found_nv; }
   }
   __syncthreads();
   if (sh_row < 0) return;   // uniform: a spare CTA of the flat grid
   const int row = sh_row;
-  const int b = row / a.n_q, iq = row % a.n_q;
-  const long long t = c.n_tokens[b] - a.n_q + iq;
-  const long long n_vis = min((t + 1) / c.m, c.cap);
+  const int b = row / a.n_q;
+  const long long n_vis = sh_nvis;
   const long long n_tiles = (n_vis + kTileM - 1) / kTileM;
   const long long tile_lo = (long long)sh_sub * n_tiles / sh_cnt;
   const long long tile_hi = (long long)(sh_sub + 1) * n_tiles / sh_cnt;
   if (tile_lo >= tile_hi) return;   // uniform: nothing allocated yet
   const int n_it = (int)(tile_hi - tile_lo);
   const int H = a.heads;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
-    for (int s = 0; s < 4; ++s) { mbar_init(&tfull[s], 1); mbar_init(&tempty[s], 4); }
-    *abort_flag = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  __syncthreads();
   const int n_acc = H <= 64 ? 4 : 2;                        // accumulator buffers (2H columns each)
   const uint32_t ncols = H <= 32 ? 256u : 512u;
   uint32_t tmem = 0;
   if (warp != 0) {
+    if (warp == 1) {   // TMEM first: it does not depend on the query
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
+                   "r"(ncols)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
     // ---- query operand (warps 1.., while warp 0 already streams keys): per-head
     //      power-of-two scale, exact e4m3 hi/lo split, written in the K-major
-    //      128-byte-swizzle layout the MMA reads
-    for (int h = warp - 1; h < H; h += kThreads / 32 - 1) {
-      float v[4];
-      const long long q0 = ((long long)row * H + h) * kDI + lane * 4;
+    //      128-byte-swizzle layout the MMA reads.  Warp w builds heads w-1, w-1+13, ...;
+    //      all of its query and weight loads are issued before the first is used, so
+    //      the build costs one memory round trip (the key stream keeps HBM queues full
+    //      by then, and a round trip per head added microseconds to every CTA's start).
+    constexpr int kQW = kThreads / 32 - 1;           // builder warps
+    constexpr int kMaxHPW = (128 + kQW - 1) / kQW;   // heads per builder warp (H <= 128)
+    const int w0 = warp - 1;
+    float4 qv[kMaxHPW];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) v[e] = load_tok(a.q_idx, a.q_dtype, q0 + e);
-      float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
-      amax = warp_max(amax);
+    for (int u = 0; u < kMaxHPW; ++u) {
+      const int h = w0 + u * kQW;
+      qv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (h < H) {
+        const long long q0 = ((long long)row * H + h) * kDI + lane * 4;
+        if (a.q_vec && a.q_dtype == CSA_BF16) {
+          const uint2 r = __ldg(reinterpret_cast<const uint2 *>(reinterpret_cast<const uint16_t *>(a.q_idx) + q0));
+          qv[u] = make_float4(__uint_as_float(r.x << 16), __uint_as_float(r.x & 0xFFFF0000u),
+                              __uint_as_float(r.y << 16), __uint_as_float(r.y & 0xFFFF0000u));
+        } else if (a.q_vec) {
+          qv[u] = __ldg(reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(a.q_idx) + q0));
+        } else {
+          qv[u] = make_float4(load_tok(a.q_idx, a.q_dtype, q0), load_tok(a.q_idx, a.q_dtype, q0 + 1),
+                              load_tok(a.q_idx, a.q_dtype, q0 + 2), load_tok(a.q_idx, a.q_dtype, q0 + 3));
+        }
+      }
+    }
+    const float wl = (lane < kMaxHPW && w0 + lane * kQW < H) ? __ldg(a.w + (long long)row * H + w0 + lane * kQW) : 0.f;
+    // loads issued: let the producer start the key stream (these small loads are then
+    // ahead of it in the memory queues instead of behind megabytes of key tiles)
+    asm volatile("bar.arrive 2, %0;" ::"n"(kThreads) : "memory");
+    // the heads of this warp go through each step together (independent chains), so
+    // the build's latency is that of one head, not of one head per step
+    float am[kMaxHPW];
+#pragma unroll
+    for (int u = 0; u < kMaxHPW; ++u)
+      am[u] = fmaxf(fmaxf(fabsf(qv[u].x), fabsf(qv[u].y)), fmaxf(fabsf(qv[u].z), fabsf(qv[u].w)));
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+#pragma unroll
+      for (int u = 0; u < kMaxHPW; ++u) am[u] = fmaxf(am[u], __shfl_xor_sync(0xffffffffu, am[u], o));
+    }
+#pragma unroll
+    for (int u = 0; u < kMaxHPW; ++u) {
+      const int h = w0 + u * kQW;
       int ex = 0;
-      frexpf(amax, &ex);
-      const float S = amax > 0.f ? ldexpf(1.f, 8 - ex) : 1.f;   // amax * S < 2^8
+      frexpf(am[u], &ex);
+      const float S = am[u] > 0.f ? ldexpf(1.f, 8 - ex) : 1.f;   // amax * S < 2^8
+      const float v[4] = {qv[u].x, qv[u].y, qv[u].z, qv[u].w};
       uint32_t hw = 0, lw = 0;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -245,19 +317,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
         hw |= (uint32_t)hi << (8 * e);
         lw |= (uint32_t)lo << (8 * e);
       }
-      const int k = lane * 4;   // 4 consecutive K bytes, inside one 16-byte chunk
-      const int off = h * kDI + ((((k >> 4) ^ (h & 7)) << 4) | (k & 15));
-      *reinterpret_cast<uint32_t *>(bhi + off) = hw;
-      *reinterpret_cast<uint32_t *>(blo + off) = lw;
-      if (lane == 0) wq[h] = a.w[(long long)row * H + h] / S;
+      const float wh = __shfl_sync(0xffffffffu, wl, u);
+      if (h < H) {
+        const int k = lane * 4;   // 4 consecutive K bytes, inside one 16-byte chunk
+        const int off = h * kDI + ((((k >> 4) ^ (h & 7)) << 4) | (k & 15));
+        *reinterpret_cast<uint32_t *>(bhi + off) = hw;
+        *reinterpret_cast<uint32_t *>(blo + off) = lw;
+        if (lane == 0) wq[h] = wh / S;
+      }
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic-proxy writes -> tensor core reads
-    if (warp == 1) {
-      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
-                   "r"(ncols)
-                   : "memory");
-      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
     tc_fence_before();
     asm volatile("bar.sync 1, %0;" ::"n"(kThreads - 32) : "memory");   // all warps but the producer
     tc_fence_after();
@@ -265,7 +334,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
   }
 
   if (warp == 0) {
+    asm volatile("bar.sync 2, %0;" ::"n"(kThreads) : "memory");   // query loads are in flight
     if (lane == 0) {   // ---- TMA producer
+      const uint64_t policy = l2_evict_first_policy();
       int issued = 0;
       for (int it = 0; it < n_it; ++it) {
         const int s = it % kStages;
@@ -274,7 +345,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
         mbar_expect_tx(&full[s], kStageBytes);
         const long long tile = tile_lo + it;
         if (c.page_size == 0) {
-          tma_load_2d(stage + s * kStageBytes, &kmap, &full[s], 0, (int)((long long)b * c.max_entries + tile * kTileM));
+          tma_load_2d(stage + s * kStageBytes, &kmap, &full[s], 0, (int)((long long)b * c.max_entries + tile * kTileM),
+                      policy);
         } else {
           for (int r0 = 0; r0 < kTileM; r0 += a.box_rows) {
             const long long j0 = tile * kTileM + r0;
@@ -282,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
             if (lp >= c.max_pages) lp = 0;   // past the table: any valid page (never scored)
             const long long pg = __ldg(c.page_table + (long long)b * c.max_pages + lp);
             tma_load_2d(stage + s * kStageBytes + r0 * kDI, &kmap, &full[s], 0,
-                        (int)(pg * c.page_size + j0 % c.page_size));
+                        (int)(pg * c.page_size + j0 % c.page_size), policy);
           }
         }
         ++issued;
@@ -376,6 +448,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
       }
     }
   }
+  // Warps 0 and 1 ran their loops on lane 0 only: reconverge each warp before the
+  // CTA barrier, which counts warps (a warp arriving in two parts would be counted
+  // twice and release the barrier while epilogue warps still read TMEM).
+  __syncwarp();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
@@ -434,11 +510,12 @@ cudaError_t launch_index_tc(const CacheView &c, int batch, int n_q, const void *
   a.c = c; a.n_q = n_q; a.heads = heads_idx; a.q_dtype = q_dtype;
   a.q_idx = (const uint8_t *)q_idx; a.w = w; a.scores = scores; a.stride = stride;
   a.box_rows = box_rows; a.status = status;
+  a.q_vec = ((uintptr_t)q_idx & 15) == 0;
   const int rows_q = batch * n_q;
   a.rows = rows_q;
   a.grid_sms = num_sms;
   dim3 grid;
-  if (rows_q >= num_sms) {   // a row per CTA
+  if (rows_q >= num_sms || rows_q > kMaxFlatRows) {   // a row per CTA
     a.ctas_per_row = 1;
     grid = dim3(1, rows_q);
   } else {                   // flat grid, CTAs split over rows by their tile counts: at most

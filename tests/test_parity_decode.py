@@ -166,3 +166,51 @@ def test_indexer_head_counts(heads_idx):
     arrs, inp = _seeded(w)
     res = H.gpu_seeded_step(w, arrs, inp)
     _check_step(w, arrs, inp, res, H.TOL_LOW, what=f"h_idx={heads_idx}")
+
+
+def _with_index_keys(w, arrs, make):
+    """Replaces every entry's indexer key bytes by make(rows) (e4m3 codes) with scale 1/64."""
+    a = dict(arrs)
+    a["idx_key"] = make(arrs["idx_key"].shape)
+    a["idx_scale"] = np.full_like(arrs["idx_scale"], 1.0 / 64.0)
+    return a
+
+
+def test_topk_all_scores_equal_uses_radix_fallback_and_lowest_indices():
+    """Identical keys give identical scores: the value histogram degenerates (min == max)
+    and the selection must fall back to the radix passes and take the lowest indices."""
+    w = S.config2(ctx=(65536, 40000, 8192, 30000), k=512)
+    arrs, inp = _seeded(w)
+    code = np.uint8(0x38)   # 1.0
+    arrs = _with_index_keys(w, arrs, lambda shape: np.full(shape, code, np.uint8))
+    res = H.gpu_seeded_step(w, arrs, inp)
+    for b in range(w.batch):
+        assert sorted(res["idx"][b, 0].tolist()) == list(range(w.k)), b
+    _check_step(w, arrs, inp, res, H.TOL_LOW, what="equal scores")
+
+
+def test_topk_crowded_threshold_bin():
+    """Two score levels, the upper one holding more than k entries: the bin of the k-th
+    score holds thousands of entries (more than the candidate list), so the selection
+    takes the radix path; ties go to the lowest indices."""
+    w = S.config2(ctx=(65536, 65536, 65536, 65536), k=1024)
+    arrs, inp = _seeded(w)
+    rng = np.random.default_rng(17)
+
+    def make(shape):
+        keys = np.full(shape, np.uint8(0x30), np.uint8)                # 0.5
+        hot = rng.random(shape[0]) < 0.3
+        keys[hot] = np.uint8(0x38)                                     # 1.0
+        return keys
+    arrs = _with_index_keys(w, arrs, make)
+    res = H.gpu_seeded_step(w, arrs, inp)
+    _check_step(w, arrs, inp, res, H.TOL_LOW, what="crowded bin")
+
+
+def test_topk_very_long_rows_take_the_global_memory_path():
+    """2^21 context tokens (524288 entries) in one row: a cluster slice would not fit in
+    shared memory, so the top-k runs the one-CTA-per-row kernel over global memory."""
+    w = S.config2(batch=1, ctx=(1 << 21,), k=2048, plant_frac=0.01)
+    arrs, inp = _seeded(w)
+    res = H.gpu_seeded_step(w, arrs, inp)
+    _check_step(w, arrs, inp, res, H.TOL_LOW, what="2M ctx")
