@@ -189,63 +189,81 @@ __global__ void __launch_bounds__(kAttThreads) k_attend(AttendArgs a) {
 }
 
 // Merge of split partials: M = max(sink, m_s), L = exp(sink-M) + sum_s l_s exp(m_s-M),
-// out = sum_s o_s exp(m_s-M) / L, lse = M + log L.  Fixed split order (each
-// element's sum runs over s = 0, 1, ... in the same order on every call).
-// The split weights are computed in parallel; each thread keeps 8 partial loads
-// in flight instead of walking the splits one memory round trip at a time.
-__global__ void __launch_bounds__(256) k_attend_combine(AttendArgs a) {
-  extern __shared__ float wts[];   // [n_splits]
-  __shared__ float red[8];
-  __shared__ float sh_M, sh_L;
-  const int h = blockIdx.x, row = blockIdx.y;
+// out = sum_s o_s exp(m_s-M) / L, lse = M + log L.  One CTA of 512 threads per
+// (row, pair of heads) -- one wave on the GPU for a decode batch -- and a thread
+// owns two adjacent output elements of one head, with up to 16 partial loads (8
+// bytes each) in flight: the merge costs a few memory round trips, not one per
+// split.  Every sum has a fixed shape (per element: s = 0, 1, ... in order; L:
+// per-thread strided sums, then a fixed tree), so the bits do not depend on
+// timing or on the batch.
+constexpr int kCombThreads = 512;
+constexpr int kCombHeads = 2;   // heads per CTA
+__global__ void __launch_bounds__(kCombThreads) k_attend_combine(AttendArgs a) {
+  extern __shared__ float wts[];   // [kCombHeads][n_splits]
+  __shared__ float red[kCombHeads][2][kCombThreads / 32];
+  const int row = blockIdx.y;
   const int d = a.c.d, S = a.n_splits;
   pdl_wait();
   pdl_trigger();
-  const float z = __ldg(a.sink + h);
-  const long long base = (long long)row * S * a.heads + h;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // M over splits and the sink
+  constexpr int NW = kCombThreads / 32;
+  // thread layout: head slot hs = tid / (kCombThreads / kCombHeads); element pair e2 within the head
+  constexpr int TPH = kCombThreads / kCombHeads;
+  const int hs = tid / TPH, t2 = tid % TPH;
+  const int h = blockIdx.x * kCombHeads + hs;
+  const bool hv = h < a.heads;
+  const long long base = (long long)row * S * a.heads + h;
+  const float z = hv ? __ldg(a.sink + h) : 0.f;
+  // per head: M and the split weights (the threads of a head are whole warps)
   float m = z;
-  for (int s = tid; s < S; s += blockDim.x) m = fmaxf(m, a.part_ml[(base + (long long)s * a.heads) * 2]);
+  if (hv)
+    for (int s = t2; s < S; s += TPH) m = fmaxf(m, a.part_ml[(base + (long long)s * a.heads) * 2]);
   m = warp_max(m);
-  if (lane == 0) red[warp] = m;
+  if (lane == 0) red[hs][0][warp % (NW / kCombHeads)] = m;
   __syncthreads();
-  if (tid == 0) {
-    float M = red[0];
-    for (int i = 1; i < (int)(blockDim.x >> 5); ++i) M = fmaxf(M, red[i]);
-    sh_M = M;
-  }
-  __syncthreads();
-  const float M = sh_M;
-  for (int s = tid; s < S; s += blockDim.x) {
-    const float ms = a.part_ml[(base + (long long)s * a.heads) * 2];
-    wts[s] = ms > -INFINITY ? expf(ms - M) : 0.f;
-  }
-  __syncthreads();
-  if (tid == 0) {   // fixed order over splits
-    float L = expf(z - M);
-    for (int s = 0; s < S; ++s) L += wts[s] * a.part_ml[(base + (long long)s * a.heads) * 2 + 1];
-    sh_L = L;
-  }
-  __syncthreads();
-  const float invL = 1.f / sh_L;
-  const long long ob = ((long long)row * a.heads + h) * d;
-  for (int e = tid; e < d; e += blockDim.x) {
-    float o = 0.f;
-    for (int s0 = 0; s0 < S; s0 += 8) {
-      float v[8];
+  float M = red[hs][0][0];
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        v[q] = (s0 + q < S && wts[s0 + q] != 0.f) ? a.part_o[(base + (long long)(s0 + q) * a.heads) * d + e] : 0.f;
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        if (s0 + q < S) o = fmaf(wts[s0 + q], v[q], o);
+  for (int i = 1; i < NW / kCombHeads; ++i) M = fmaxf(M, red[hs][0][i]);
+  float lp = 0.f;
+  if (hv)
+    for (int s = t2; s < S; s += TPH) {
+      const float ms = a.part_ml[(base + (long long)s * a.heads) * 2];
+      const float ws = ms > -INFINITY ? expf(ms - M) : 0.f;
+      wts[hs * S + s] = ws;
+      lp = fmaf(ws, a.part_ml[(base + (long long)s * a.heads) * 2 + 1], lp);
     }
-    o *= invL;
-    if (a.out_dtype == CSA_F32) reinterpret_cast<float *>(a.out)[ob + e] = o;
-    else reinterpret_cast<uint16_t *>(a.out)[ob + e] = f32_to_bf16_rn(o);
+  lp = warp_sum(lp);
+  if (lane == 0) red[hs][1][warp % (NW / kCombHeads)] = lp;
+  __syncthreads();
+  float L = expf(z - M);
+#pragma unroll
+  for (int i = 0; i < NW / kCombHeads; ++i) L += red[hs][1][i];
+  const float invL = 1.f / L;
+  const float *w = wts + hs * S;
+  for (int e = 2 * t2; hv && e < d; e += 2 * TPH) {
+    float o0 = 0.f, o1 = 0.f;
+    for (int s0 = 0; s0 < S; s0 += 16) {
+      float2 v[16];
+#pragma unroll
+      for (int q = 0; q < 16; ++q)
+        v[q] = (s0 + q < S && w[s0 + q] != 0.f)
+                   ? *reinterpret_cast<const float2 *>(a.part_o + (base + (long long)(s0 + q) * a.heads) * d + e)
+                   : make_float2(0.f, 0.f);
+#pragma unroll
+      for (int q = 0; q < 16; ++q)
+        if (s0 + q < S) {
+          o0 = fmaf(w[s0 + q], v[q].x, o0);
+          o1 = fmaf(w[s0 + q], v[q].y, o1);
+        }
+    }
+    o0 *= invL;
+    o1 *= invL;
+    const long long ob = ((long long)row * a.heads + h) * d + e;
+    if (a.out_dtype == CSA_F32) *reinterpret_cast<float2 *>(reinterpret_cast<float *>(a.out) + ob) = make_float2(o0, o1);
+    else *reinterpret_cast<uint32_t *>(reinterpret_cast<uint16_t *>(a.out) + ob) =
+             (uint32_t)f32_to_bf16_rn(o0) | ((uint32_t)f32_to_bf16_rn(o1) << 16);
   }
-  if (tid == 0 && a.out_lse) a.out_lse[(long long)row * a.heads + h] = sh_M + logf(sh_L);
+  if (hv && t2 == 0 && a.out_lse) a.out_lse[(long long)row * a.heads + h] = M + logf(L);
 }
 
 // Split plan shared by the launcher and the workspace sizing.  It depends only
@@ -282,7 +300,8 @@ cudaError_t launch_attend(const AttendArgs &a0, int rows, cudaStream_t st) {
 }
 
 cudaError_t launch_attend_combine(const AttendArgs &a, int rows, cudaStream_t st) {
-  return launch_pdl(k_attend_combine, dim3(a.heads, rows), dim3(256), a.n_splits * sizeof(float), st, 1, a);
+  return launch_pdl(k_attend_combine, dim3((a.heads + kCombHeads - 1) / kCombHeads, rows), dim3(kCombThreads),
+                    kCombHeads * a.n_splits * sizeof(float), st, 1, a);
 }
 
 }  // namespace csa

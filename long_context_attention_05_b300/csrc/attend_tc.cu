@@ -79,6 +79,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttendArgs a) {
   float *corr = l_run + kHeadsMax;
   long long *ksrc = reinterpret_cast<long long *>(corr + kHeadsMax);    // [64]
   float2 *qcs = reinterpret_cast<float2 *>(ksrc + kKeys);               // [32] (cos, sin) at t
+  float2 *wcs = qcs + 32;                                                // [64][32] window tokens' (cos, sin)
 
   const CacheView &c = a.c;
   const int row = blockIdx.y;
@@ -92,8 +93,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttendArgs a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = warp & 3, qq = warp >> 2;
 
-  // key source of slot tid of a chunk: entry row (>= 0), -2 - position (window
-  // token) or -1 (no key); sigma as described above
+  // key source of slot tid of a chunk: entry row (>= 0), -2 - ring row (window
+  // token; the ring slot is resolved here, once per key, not per gathered piece)
+  // or -1 (no key); sigma as described above
   auto key_src = [&](long long u0) {
     const long long u = u0 + tid;
     long long src = -1;
@@ -102,7 +104,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttendArgs a) {
       if (j >= 0 && j < n_vis) src = entry_row(c, b, j);
     } else if (u < U) {
       const long long tau = t - c.n_win + 1 + (u - n_list);
-      if (tau >= 0) src = -2 - tau;
+      if (tau >= 0) src = -2 - ((long long)b * c.win_cap + tau % c.win_cap);
     }
     return src;
   };
@@ -125,8 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttendArgs a) {
           else if (p < NOPE16 + ROPE16)
             buf[r] = __ldg(reinterpret_cast<const uint4 *>(c.kv_rope + src * 64 * 2) + (p - NOPE16));
         } else if (src <= -2 && p < RAW16) {
-          const long long tau = -2 - src;
-          buf[r] = __ldg(reinterpret_cast<const uint4 *>(c.win + ((long long)b * c.win_cap + tau % c.win_cap) * D * 2) + p);
+          buf[r] = __ldg(reinterpret_cast<const uint4 *>(c.win + (-2 - src) * D * 2) + p);
         }
       }
     }
@@ -160,7 +161,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttendArgs a) {
         }
       } else if (src <= -2) {
         if (p < RAW16) {
-          const long long tau = -2 - src;
           const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
           float f[8];
 #pragma unroll
@@ -171,11 +171,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttendArgs a) {
           if (p * 8 >= DN) {   // rotary dims of a window token turn at its position
 #pragma unroll
             for (int e = 0; e < 8; e += 2) {
-              float cs, sn;
-              rope_cos_sin(tau, a.rope.step[(p * 8 + e - DN) >> 1], cs, sn);
+              const float2 cs = wcs[kk * 32 + ((p * 8 + e - DN) >> 1)];
               const float x0 = f[e], x1 = f[e + 1];
-              f[e] = fmaf(x0, cs, -x1 * sn);
-              f[e + 1] = fmaf(x0, sn, x1 * cs);
+              f[e] = fmaf(x0, cs.x, -x1 * cs.y);
+              f[e + 1] = fmaf(x0, cs.y, x1 * cs.x);
             }
           }
           uint4 o;
@@ -185,6 +184,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttendArgs a) {
         }
       } else if (p < RAW16) {
         *reinterpret_cast<uint4 *>(dst + p * 8) = make_uint4(0, 0, 0, 0);
+      }
+    }
+  };
+
+  // (cos, sin) of every rotary pair of the chunk's window tokens, spread over all
+  // threads (4 each) instead of falling on the few threads that hold rotary pieces
+  auto win_rope = [&](long long u0) {
+#pragma unroll
+    for (int r = 0; r < kKeys * 32 / kThreads; ++r) {
+      const int e = tid + r * kThreads, kk = e >> 5, pr = e & 31;
+      if (ksrc[kk] <= -2) {
+        const long long tau = t - c.n_win + 1 + (u0 + kk - n_list);   // the token's position
+        float cs, sn;
+        rope_cos_sin(tau, a.rope.step[pr], cs, sn);
+        wcs[e] = make_float2(cs, sn);
       }
     }
   };
@@ -230,65 +244,101 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttendArgs a) {
   __syncthreads();   // ksrc, qcs visible
   uint4 gbuf[kGatherPer];
   gather_load(gbuf);
+  const bool win0 = ch0 * kKeys < U && ch0 * kKeys + kKeys > n_list;   // uniform: window tokens in chunk 0
+  if (win0) win_rope(ch0 * kKeys);
   {
+    // The heads of this warp go through each step together, QG at a time
+    // (independent chains: a group costs the latency of one head, not of QG).
     constexpr int PER = D / 32;
+    constexpr int QG = QH;
 #pragma unroll
-    for (int hh = 0; hh < QH; ++hh) {
-      const int h = warp + hh * (kThreads / 32);
-      float v[PER];
+    for (int hg = 0; hg < QH; hg += QG) {
+    float v[QG][PER];
+#pragma unroll
+    for (int hh = 0; hh < QG; ++hh) {
+      const int h = warp + (hg + hh) * (kThreads / 32);
       if (h < H) {
         const long long q0 = ((long long)row * H + h) * D + lane * PER;
         if (a.q_dtype == CSA_BF16 && PER % 8 == 0) {   // from the 16-byte loads issued above
 #pragma unroll
           for (int u = 0; u < PER / 8; ++u) {
-            const uint4 x = qraw[hh][u];
+            const uint4 x = qraw[hg + hh][u];
             const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              v[u * 8 + 2 * e] = bf16_bits_to_f32((uint16_t)(w4[e] & 0xFFFF));
-              v[u * 8 + 2 * e + 1] = bf16_bits_to_f32((uint16_t)(w4[e] >> 16));
+              v[hh][u * 8 + 2 * e] = bf16_bits_to_f32((uint16_t)(w4[e] & 0xFFFF));
+              v[hh][u * 8 + 2 * e + 1] = bf16_bits_to_f32((uint16_t)(w4[e] >> 16));
             }
           }
         } else if (a.q_dtype == CSA_BF16 && PER == 4) {   // d = 128: one 8-byte load
           const uint2 x = __ldg(reinterpret_cast<const uint2 *>(reinterpret_cast<const uint16_t *>(a.q) + q0));
-          v[0] = bf16_bits_to_f32((uint16_t)(x.x & 0xFFFF));
-          v[1] = bf16_bits_to_f32((uint16_t)(x.x >> 16));
-          v[2] = bf16_bits_to_f32((uint16_t)(x.y & 0xFFFF));
-          v[3] = bf16_bits_to_f32((uint16_t)(x.y >> 16));
+          v[hh][0] = bf16_bits_to_f32((uint16_t)(x.x & 0xFFFF));
+          v[hh][1] = bf16_bits_to_f32((uint16_t)(x.x >> 16));
+          v[hh][2] = bf16_bits_to_f32((uint16_t)(x.y & 0xFFFF));
+          v[hh][3] = bf16_bits_to_f32((uint16_t)(x.y >> 16));
         } else {
 #pragma unroll
-          for (int e = 0; e < PER; ++e) v[e] = load_tok(a.q, a.q_dtype, q0 + e);
-        }
-        // rotary turn of the pairs this lane holds (last 64 dims)
-#pragma unroll
-        for (int e = 0; e < PER; e += 2) {
-          const int dim = lane * PER + e;
-          if (dim >= DN) {
-            const float2 cs = qcs[(dim - DN) >> 1];
-            const float x0 = v[e], x1 = v[e + 1];
-            v[e] = fmaf(x0, cs.x, -x1 * cs.y);
-            v[e + 1] = fmaf(x0, cs.y, x1 * cs.x);
-          }
+          for (int e = 0; e < PER; ++e) v[hh][e] = load_tok(a.q, a.q_dtype, q0 + e);
         }
       } else {
 #pragma unroll
-        for (int e = 0; e < PER; ++e) v[e] = 0.f;
+        for (int e = 0; e < PER; ++e) v[hh][e] = 0.f;
       }
-      float amax = 0.f;
+    }
+    // rotary turn of the pairs this lane holds (last 64 dims)
+    if (lane * PER + PER > DN) {
 #pragma unroll
-      for (int e = 0; e < PER; ++e) amax = fmaxf(amax, fabsf(v[e]));
-      amax = warp_max(amax);
+      for (int e = 0; e < PER; e += 2) {
+        const int dim = lane * PER + e;
+        if (dim >= DN) {
+          const float2 cs = qcs[(dim - DN) >> 1];
+#pragma unroll
+          for (int hh = 0; hh < QG; ++hh) {
+            const float x0 = v[hh][e], x1 = v[hh][e + 1];
+            v[hh][e] = fmaf(x0, cs.x, -x1 * cs.y);
+            v[hh][e + 1] = fmaf(x0, cs.y, x1 * cs.x);
+          }
+        }
+      }
+    }
+    float am[QG];
+#pragma unroll
+    for (int hh = 0; hh < QG; ++hh) {
+      am[hh] = 0.f;
+#pragma unroll
+      for (int e = 0; e < PER; ++e) am[hh] = fmaxf(am[hh], fabsf(v[hh][e]));
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+#pragma unroll
+      for (int hh = 0; hh < QG; ++hh) am[hh] = fmaxf(am[hh], __shfl_xor_sync(0xffffffffu, am[hh], o));
+    }
+#pragma unroll
+    for (int hh = 0; hh < QG; ++hh) {
+      const int h = warp + (hg + hh) * (kThreads / 32);
       int ex = 0;
-      frexpf(amax, &ex);
-      const float S = amax > 0.f ? ldexpf(1.f, 14 - ex) : 1.f;
-      uint32_t *dst = reinterpret_cast<uint32_t *>(Qs + h * LDQ + lane * PER);
+      frexpf(am[hh], &ex);
+      const float S = am[hh] > 0.f ? ldexpf(1.f, 14 - ex) : 1.f;
+      // 16-byte (or 8-byte) stores: a lane's PER halves are contiguous, and 4-byte
+      // stores at a 2*PER-byte lane stride would conflict PER/2 ways
+      uint32_t pk[PER / 2];
 #pragma unroll
-      for (int e = 0; e < PER; e += 2) dst[e / 2] = pack_h2(v[e] * S, v[e + 1] * S);
+      for (int e = 0; e < PER; e += 2) pk[e / 2] = pack_h2(v[hh][e] * S, v[hh][e + 1] * S);
+      if constexpr (PER % 8 == 0) {
+        uint4 *dst = reinterpret_cast<uint4 *>(Qs + h * LDQ + lane * PER);
+#pragma unroll
+        for (int u = 0; u < PER / 8; ++u) dst[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+      } else {
+        uint2 *dst = reinterpret_cast<uint2 *>(Qs + h * LDQ + lane * PER);
+#pragma unroll
+        for (int u = 0; u < PER / 4; ++u) dst[u] = make_uint2(pk[2 * u], pk[2 * u + 1]);
+      }
       if (lane == 0) {
         qsc[h] = a.scale / S;
         m_run[h] = -INFINITY;
         l_run[h] = 0.f;
       }
+    }
     }
   }
 
@@ -301,6 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttendArgs a) {
       sig_next = src_next >= 0 ? 256.f * __ldg(c.kv_scale + src_next) : (src_next <= -2 ? 1.f : 0.f);
     }
   }
+  if (win0) __syncthreads();   // window (cos, sin) table visible
   gather_store(gbuf);
 
   float acc[NT][4];
@@ -327,6 +378,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttendArgs a) {
       }
       __syncthreads();
       gather_load(gbuf);
+      if (u0 + kKeys > n_list) {   // uniform
+        win_rope(u0);
+        __syncthreads();
+      }
       gather_store(gbuf);
       __syncthreads();
     }
@@ -491,7 +546,8 @@ bool attend_tc_supported(const CacheView &c, int heads, int q_dtype) {
 
 size_t attend_tc_smem_bytes(int d) {
   return (size_t)(2 * kHeadsMax * (d + kPadH)) * 2 + (size_t)kHeadsMax * (kKeys + 4) * 4 +
-         (size_t)2 * kHeadsMax * (kKeys + kPadH) * 2 + (size_t)(kKeys + 4 * kHeadsMax) * 4 + kKeys * 8 + 32 * 8;
+         (size_t)2 * kHeadsMax * (kKeys + kPadH) * 2 + (size_t)(kKeys + 4 * kHeadsMax) * 4 + kKeys * 8 + 32 * 8 +
+         (size_t)kKeys * 32 * 8;
 }
 
 cudaError_t launch_attend_tc(const AttendArgs &a, int rows, cudaStream_t st) {

@@ -438,8 +438,11 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_cluster(CacheView c, int 
   }
   // prefix = T, the k-th largest key; krem keys equal to T are still to be taken.
   // Warp w owns the contiguous run [w*seg, (w+1)*seg) of this slice and walks it
-  // 32 keys at a time (coalesced, conflict-free); ballots order keys inside a
-  // round, one block scan orders the warps.
+  // once, 32 keys at a time (coalesced, conflict-free): it counts the keys > T and
+  // == T and compacts their slice positions, in index order, to the front of its
+  // own run (in place: a round writes only below the keys it has read; bit 31
+  // marks a key == T).  One block scan orders the warps; the output pass then walks
+  // only the compacted lists.
   const unsigned lt = (1u << lane) - 1u;
   const int seg = ((len + nwarps - 1) / nwarps + 31) & ~31;
   const int w0 = min(len, warp * seg), w1 = min(len, w0 + seg);
@@ -447,8 +450,12 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_cluster(CacheView c, int 
   for (int j0 = w0; j0 < w1; j0 += 32) {
     const int j = j0 + lane;
     const unsigned key = j < w1 ? keys[j] : 0u;
-    gw += __popc(__ballot_sync(0xffffffffu, j < w1 && key > prefix));
-    ew += __popc(__ballot_sync(0xffffffffu, j < w1 && key == prefix));
+    const bool isg = j < w1 && key > prefix, ise = j < w1 && key == prefix;
+    const unsigned bg = __ballot_sync(0xffffffffu, isg), be = __ballot_sync(0xffffffffu, ise);
+    const unsigned bs = bg | be;
+    if (isg || ise) keys[w0 + gw + ew + __popc(bs & lt)] = (unsigned)j | (ise ? 0x80000000u : 0u);
+    gw += __popc(bg);
+    ew += __popc(be);
   }
   int tot;
   const int ex = block_exclusive_scan(lane == 0 ? ((ew << 16) | gw) : 0, scan_buf, tot);   // counts < 2^16
@@ -480,14 +487,15 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_cluster(CacheView c, int 
   const int limit = max(0, krem - eq_before);   // equal keys this CTA may take, in index order
   int e_seen = wex >> 16;                        // equal keys before this warp's run (in this CTA)
   long long pos = base + (wex & 0xFFFF) + min(limit, e_seen);
-  for (int j0 = w0; j0 < w1; j0 += 32) {
-    const int j = j0 + lane;
-    const unsigned key = j < w1 ? keys[j] : 0u;
-    const bool isg = j < w1 && key > prefix, ise = j < w1 && key == prefix;
+  const int nw = gw + ew;                        // this warp's compacted list: keys[w0, w0 + nw)
+  for (int i0 = 0; i0 < nw; i0 += 32) {
+    const int i = i0 + lane;
+    const unsigned ent = i < nw ? keys[w0 + i] : 0u;
+    const bool ise = i < nw && (ent >> 31) != 0u, isg = i < nw && !ise;
     const unsigned be = __ballot_sync(0xffffffffu, ise);
     const bool take = isg || (ise && e_seen + __popc(be & lt) < limit);
     const unsigned bt = __ballot_sync(0xffffffffu, take);
-    if (take) out[pos + __popc(bt & lt)] = (int32_t)(lo + j);
+    if (take) out[pos + __popc(bt & lt)] = (int32_t)(lo + (ent & 0x7FFFFFFFu));
     pos += __popc(bt);
     e_seen += __popc(be);
   }
