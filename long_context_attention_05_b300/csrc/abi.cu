@@ -140,6 +140,15 @@ size_t scores_bytes(const csa_cache *c, int batch, int n_q) {
   return align256((size_t)batch * n_q * entry_cap(c) * sizeof(float));
 }
 
+// Prefix histograms of a fused index + top-k call (decode-sized calls only) sit at the
+// end of the workspace, 256-byte aligned, clear of the scores and of the attention's
+// split partials (both start after the header); csa_workspace_size reserves them.
+// 0 bytes when the call has too many rows for them.
+size_t hist_bytes(int batch, int n_q) {
+  const long long rows = (long long)batch * n_q;
+  return rows <= csa::kPrefixRowsMax ? (size_t)rows * csa::kPrefixBins * sizeof(unsigned) : 0;
+}
+
 csa_status check_ws(void *ws, size_t ws_bytes, size_t need) {
   if (need == 0) return ok();
   if (!ws) return fail(CSA_ERR_WORKSPACE, "workspace is NULL (need %zu bytes)", need);
@@ -201,12 +210,18 @@ csa_status check_index_args(const csa_cache *c, int batch, int n_q, const void *
 
 // Indexer dispatch: the tensor-core kernel for e4m3 keys of dim 128 and 32/64/128
 // heads; the CUDA-core kernel otherwise (fp32 caches, other dims).
+// hist (may be null): per-row prefix histograms for the top-k, filled only by the
+// tensor-core indexer; *hist_used tells the caller whether they were filled
 cudaError_t launch_indexer(const csa_cache *c, int batch, int n_q, const void *q_idx, int q_dtype, const float *w,
-                           int heads_idx, float *scores, long long stride, void *ws, cudaStream_t st) {
+                           int heads_idx, float *scores, long long stride, void *ws, cudaStream_t st,
+                           unsigned *hist = nullptr, bool *hist_used = nullptr) {
   const csa::CacheView v = view(c);
-  if (csa::index_tc_supported(v, heads_idx))
+  if (hist_used) *hist_used = false;
+  if (csa::index_tc_supported(v, heads_idx)) {
+    if (hist_used) *hist_used = hist != nullptr;
     return csa::launch_index_tc(v, batch, n_q, q_idx, q_dtype, w, heads_idx, scores, stride, num_sms(),
-                                ws ? (int *)ws : nullptr, st);
+                                ws ? (int *)ws : nullptr, hist, st);
+  }
   return csa::launch_index_generic(v, batch, n_q, q_idx, q_dtype, w, heads_idx, scores, stride, entry_cap(c), st);
 }
 
@@ -257,6 +272,7 @@ size_t csa_workspace_size(const csa_cache *c, int batch, int n_q, int heads, int
   if (k > 0) need = std::max(need, kHeader + scores_bytes(c, batch, n_q));
   const AttendPlan p = attend_plan(c, batch, n_q, heads, k > 0 ? (long long)k : entry_cap(c));
   need = std::max(need, kHeader + p.part_o_bytes + p.part_ml_bytes);
+  if (k > 0) need = ((need + 255) & ~(size_t)255) + hist_bytes(batch, n_q);
   return need;
 }
 
@@ -299,7 +315,7 @@ csa_status csa_topk(const csa_cache *c, int batch, int n_q, const float *scores,
   if (k < 1) return fail(CSA_ERR_INVALID_ARG, "k must be >= 1");
   if (!scores || !out_idx || !out_count) return fail(CSA_ERR_INVALID_ARG, "NULL pointer");
   if (stride < 1) return fail(CSA_ERR_INVALID_ARG, "scores_stride must be >= 1");
-  return cuda_status(csa::launch_topk(view(c), batch, n_q, scores, stride, k, out_idx, out_count, num_sms(),
+  return cuda_status(csa::launch_topk(view(c), batch, n_q, scores, stride, k, out_idx, out_count, nullptr, num_sms(),
                                       (cudaStream_t)stream),
                      "top-k launch");
 }
@@ -315,9 +331,16 @@ csa_status csa_index_topk(const csa_cache *c, int batch, int n_q, const void *q_
   if ((s = check_ws(ws, ws_bytes, need))) return s;
   float *scores = (float *)((char *)ws + kHeader);
   const long long cap = entry_cap(c);
-  cudaError_t e = launch_indexer(c, batch, n_q, q_idx, q_dtype, w, heads_idx, scores, cap, ws, (cudaStream_t)stream);
+  // prefix histograms when the workspace has room for them (sized by csa_workspace_size)
+  const size_t hb = hist_bytes(batch, n_q);
+  const size_t ho = ws_bytes >= hb ? (ws_bytes - hb) & ~(size_t)255 : 0;
+  unsigned *hist = hb && ho >= need ? (unsigned *)((char *)ws + ho) : nullptr;
+  bool used = false;
+  cudaError_t e = launch_indexer(c, batch, n_q, q_idx, q_dtype, w, heads_idx, scores, cap, ws, (cudaStream_t)stream,
+                                 hist, &used);
   if (e != cudaSuccess) return cuda_status(e, "indexer launch");
-  return cuda_status(csa::launch_topk(view(c), batch, n_q, scores, cap, k, out_idx, out_count, num_sms(), (cudaStream_t)stream),
+  return cuda_status(csa::launch_topk(view(c), batch, n_q, scores, cap, k, out_idx, out_count, used ? hist : nullptr,
+                                      num_sms(), (cudaStream_t)stream),
                      "top-k launch");
 }
 
@@ -341,7 +364,7 @@ csa_status csa_index_topk_static(const csa_cache *c, int batch, int n_q, const v
   const long long cap = entry_cap(c);
   e = launch_indexer(c, batch, n_q, q_idx, q_dtype, w, heads_idx, scores, cap, ws, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_status(e, "indexer launch");
-  return cuda_status(csa::launch_topk(view(c), batch, n_q, scores, cap, k, out_idx, out_count, num_sms(),
+  return cuda_status(csa::launch_topk(view(c), batch, n_q, scores, cap, k, out_idx, out_count, nullptr, num_sms(),
                                       (cudaStream_t)stream),
                      "top-k launch");
 }

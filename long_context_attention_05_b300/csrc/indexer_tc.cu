@@ -60,6 +60,7 @@ struct TcArgs {
   int box_rows;       // rows per TMA box: 128 (contiguous) or the page size
   int *status;        // workspace status word (may be null)
   int q_vec;          // q_idx is 16-byte aligned: vector loads of the query
+  unsigned *hist;     // per-row histograms of score-key prefixes (kPrefixBins each), or null
 };
 
 __device__ __forceinline__ uint32_t su32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -160,6 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
   uint64_t *tempty = tfull + 4;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 4);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  unsigned *shist = reinterpret_cast<unsigned *>(reinterpret_cast<uint8_t *>(tempty + 4) + 16);   // [kPrefixBins]
 
   const CacheView &c = a.c;
   // ---- work assignment.  Many query rows (>= one per SM): CTA y takes row y.
@@ -180,6 +182,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
   auto visible = [&](long long n_tok, int r) {   // entries query row r sees
     return min((n_tok - a.n_q + r % a.n_q + 1) / c.m, c.cap);
   };
+  if (a.hist)
+    for (int e = threadIdx.x; e < kPrefixBins; e += kThreads) shist[e] = 0u;
   if (a.ctas_per_row > 0) {
     if (threadIdx.x == 0) {
       sh_row = blockIdx.y; sh_sub = blockIdx.x; sh_cnt = a.ctas_per_row;
@@ -443,7 +447,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
         if (lane == 0) mbar_arrive(&tempty[acc]);
         const float sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
         const long long j = (tile_lo + it) * kTileM + g * 32 + lane;
-        if (j < n_vis) a.scores[(long long)row * a.stride + j] = sum * sc[u];
+        if (j < n_vis) {
+          const float v = sum * sc[u];
+          a.scores[(long long)row * a.stride + j] = v;
+          if (a.hist) atomicAdd(&shist[float_key(v) >> (32 - kPrefixBits)], 1u);
+        }
         sc[u] = scale_of(it + 4 * n_grp);
       }
     }
@@ -453,6 +461,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
   // twice and release the barrier while epilogue warps still read TMEM).
   __syncwarp();
   __syncthreads();
+  if (a.hist) {   // this CTA's prefix counts into the row's histogram
+    for (int e = threadIdx.x; e < kPrefixBins; e += kThreads) {
+      const unsigned v = shist[e];
+      if (v) atomicAdd(a.hist + (long long)row * kPrefixBins + e, v);
+    }
+  }
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
@@ -485,12 +499,13 @@ bool index_tc_supported(const CacheView &c, int heads_idx) {
 }
 
 size_t index_tc_smem_bytes() {
-  return 1024 + (size_t)kStages * kStageBytes + 2 * 128 * kDI + 128 * sizeof(float) + (2 * kStages + 8) * 8 + 16;
+  return 1024 + (size_t)kStages * kStageBytes + 2 * 128 * kDI + 128 * sizeof(float) + (2 * kStages + 8) * 8 + 16 +
+         (size_t)kPrefixBins * sizeof(unsigned);
 }
 
 cudaError_t launch_index_tc(const CacheView &c, int batch, int n_q, const void *q_idx, int q_dtype, const float *w,
                             int heads_idx, float *scores, long long stride, int num_sms, int *status,
-                            cudaStream_t st) {
+                            unsigned *hist, cudaStream_t st) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   CUtensorMap map;
@@ -511,6 +526,7 @@ cudaError_t launch_index_tc(const CacheView &c, int batch, int n_q, const void *
   a.q_idx = (const uint8_t *)q_idx; a.w = w; a.scores = scores; a.stride = stride;
   a.box_rows = box_rows; a.status = status;
   a.q_vec = ((uintptr_t)q_idx & 15) == 0;
+  a.hist = hist;
   const int rows_q = batch * n_q;
   a.rows = rows_q;
   a.grid_sms = num_sms;

@@ -46,10 +46,17 @@ bool index_tc_supported(const CacheView &c, int heads_idx);
 size_t index_tc_smem_bytes();
 cudaError_t launch_index_tc(const CacheView &c, int batch, int n_q, const void *q_idx, int q_dtype, const float *w,
                             int heads_idx, float *scores, long long stride, int num_sms, int *status,
-                            cudaStream_t st);
+                            unsigned *hist, cudaStream_t st);
+
+// Histogram of the top kPrefixBits bits of the order-preserving score keys, one per
+// query row: the tensor-core indexer fills it (when given one) while it scores, and
+// the cluster top-k reads it to find the bin of the k-th largest score, then zeroes it.
+constexpr int kPrefixBits = 13;
+constexpr int kPrefixBins = 1 << kPrefixBits;
+constexpr int kPrefixRowsMax = 256;   // rows served with prefix histograms (decode-sized calls)
 
 cudaError_t launch_topk(const CacheView &c, int batch, int n_q, const float *scores, long long stride, int k,
-                        int32_t *out_idx, int32_t *out_count, int num_sms, cudaStream_t st);
+                        int32_t *out_idx, int32_t *out_count, unsigned *hist, int num_sms, cudaStream_t st);
 
 constexpr int kHG = 16;
 constexpr int kKC = 32;

@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_row(CacheView c, int n_q,
 // passes over the ordered-integer keys.  Every decision is integer counting on
 // identical data in every CTA, so the result is deterministic.
 constexpr int kBins = 2048;
-constexpr int kCandMax = 2048;
+constexpr int kCandMax = 4096;   // threshold-bin keys resolved without a pass over every key
 
 __device__ __forceinline__ float key_float(unsigned key) {
   return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
@@ -145,7 +145,7 @@ __device__ __forceinline__ float key_float(unsigned key) {
 
 __global__ void __launch_bounds__(kTopkThreads) k_topk_cluster(CacheView c, int n_q, const float *scores,
                                                                long long stride, int k, int32_t *out_idx,
-                                                               int32_t *out_count, int slice_cap) {
+                                                               int32_t *out_count, unsigned *ghist, int slice_cap) {
   namespace cg = cooperative_groups;
   cg::cluster_group cl = cg::this_cluster();
   extern __shared__ unsigned keys[];             // [slice_cap] keys, then [slice_cap] uint16 bins
@@ -163,6 +163,7 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_cluster(CacheView c, int 
   __shared__ unsigned sh_prefix;
   __shared__ int sh_krem, sh_bin, sh_above, sh_incount;
   __shared__ int cnt[2];                         // this CTA's (greater, equal) counts
+  __shared__ int sh_myab;                        // fast path: this CTA's keys above the threshold bin
   const int CS = (int)cl.num_blocks();
   const int rank = (int)cl.block_rank();
   const int row = blockIdx.y;
@@ -236,156 +237,286 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_cluster(CacheView c, int 
     z = __reduce_max_sync(0xffffffffu, z);
     if (lane == 0) { sh_minmax[0] = a; sh_minmax[1] = z; }
   }
-  cl.sync();   // S1: every CTA's (min, max) visible; every part[] / counter zeroed
-  unsigned gmin = 0xFFFFFFFFu, gmax = 0u;
+  // ---- fast path: the indexer left this row's histogram of 13-bit key prefixes (bins
+  //      of 1/16 octave).  If it counts exactly this row's n scores, the bin of the
+  //      k-th largest key and the count above it come straight from it: no min / max,
+  //      no histogram pass, no cluster exchange of histograms.
+  bool fast = false;
+  if (ghist != nullptr) {   // uniform
+    static_assert(kPrefixBins == 8 * kTopkThreads, "one thread per 8 prefix bins");
+    const unsigned *hr = ghist + (long long)row * kPrefixBins;
+    const int hb = kPrefixBins - 8 * ((int)threadIdx.x + 1);   // this thread's bins hb .. hb+7
+    const uint4 h0 = *reinterpret_cast<const uint4 *>(hr + hb), h1 = *reinterpret_cast<const uint4 *>(hr + hb + 4);
+    const unsigned cb[8] = {h1.w, h1.z, h1.y, h1.x, h0.w, h0.z, h0.y, h0.x};   // descending bins
+    int s8 = 0;
 #pragma unroll
-  for (int r = 0; r < 16; ++r) {
-    if (r < CS) {
-      const unsigned *mm = cl.map_shared_rank(sh_minmax, r);
-      gmin = min(gmin, mm[0]);
-      gmax = max(gmax, mm[1]);
+    for (int q = 0; q < 8; ++q) s8 += (int)cb[q];
+    int tot;
+    const int above = block_exclusive_scan(s8, scan_buf, tot);   // keys in higher bins
+    if ((long long)tot == n && above < k && above + s8 >= k) {
+      int cum = above;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (cum < k && cum + (int)cb[q] >= k) { sh_bin = hb + 7 - q; sh_above = cum; sh_incount = (int)cb[q]; }
+        cum += (int)cb[q];
+      }
     }
+    fast = (long long)tot == n;   // the same in every thread and every CTA of the row
+    __syncthreads();
   }
-  const float vmin = key_float(gmin), vmax = key_float(gmax);
-  const float scale = (float)kBins / (vmax - vmin);
-  const bool binned = gmax > gmin && isfinite(scale) && scale > 0.f && isfinite(vmin) && isfinite(vmax);
   unsigned prefix = 0;
   int krem = k;
-  bool need_radix = !binned;
-  bool fast_offsets = false;   // output offsets known from rank 0's lists (no count exchange)
-  if (binned) {
-    // ---- value histogram (bin(v) is monotone in v); non-empty bins are added
-    //      straight into the owner CTA's merged array
-    const int per = kBins / CS;
-    unsigned *hsub = hist[warp & 3];
-    for (int j = threadIdx.x; j < len; j += blockDim.x) {
-      const int bin = min(kBins - 1, (int)((key_float(keys[j]) - vmin) * scale));
-      kbin[j] = (unsigned short)bin;
-      atomicAdd(&hsub[bin], 1u);
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e < kBins; e += blockDim.x) {
-      const unsigned v = hist[0][e] + hist[1][e] + hist[2][e] + hist[3][e];
-      hist[0][e] = v;
-      if (v) atomicAdd(cl.map_shared_rank(part, e / per) + e, v);
-    }
-    cl.sync();   // S2: merged histogram complete
-    // thread x owns bins 2047-2x and 2046-2x (descending)
-    const int b0 = kBins - 1 - 2 * (int)threadIdx.x, b1 = b0 - 1;
-    const unsigned c0 = cl.map_shared_rank(part, b0 / per)[b0];
-    const unsigned c1 = cl.map_shared_rank(part, b1 / per)[b1];
-    int tot;
-    const int above = block_exclusive_scan((int)(c0 + c1), scan_buf, tot);   // keys in higher bins
-    if (above < k && above + (int)(c0 + c1) >= k) {
-      const bool first = above + (int)c0 >= k;
-      sh_bin = first ? b0 : b1;
-      sh_above = first ? above : above + (int)c0;
-      sh_incount = (int)(first ? c0 : c1);
-    }
-    __syncthreads();
-    const int bstar = sh_bin, kin = k - sh_above, total = sh_incount;
-    if (total <= kCandMax) {
-      // ---- the threshold bin's keys of every CTA (with their rank) and every CTA's
-      //      count of keys above the bin go to rank 0
-      unsigned *cand0 = cl.map_shared_rank(cand, 0);
-      unsigned char *crank0 = cl.map_shared_rank(cand_rank, 0);
-      int *cnt0 = cl.map_shared_rank(&sh_cand, 0);
-      for (int j = threadIdx.x; j < len; j += blockDim.x)
-        if (kbin[j] == bstar) {
-          const int slot = atomicAdd(cnt0, 1);
-          cand0[slot] = keys[j];
-          crank0[slot] = (unsigned char)rank;
+  bool need_radix = false;
+  bool fast_offsets = false;   // output offsets known from the candidate lists (no count exchange)
+  bool fast_list = false;      // this warp's keys in or above the threshold bin are listed in kbin
+  int nsel = 0;                // ... that many
+  // Warp w owns the contiguous run [w*seg, (w+1)*seg) of this slice in the passes
+  // below that must keep index order; it walks it 32 keys at a time (coalesced,
+  // conflict-free) and ballots order the keys inside a round.
+  const unsigned lt = (1u << lane) - 1u;
+  const int seg = ((len + nwarps - 1) / nwarps + 31) & ~31;
+  const int w0 = min(len, warp * seg), w1 = min(len, w0 + seg);
+  // exact k-th key T among the threshold bin's candidates ck[0, total) (rank cr[x]
+  // each), and per rank the candidates above T and equal to T
+  // (pre0, msk0): bits every candidate shares; the radix passes cover the rest
+  auto select_among = [&](const unsigned *ck, const unsigned char *cr, int total, int kin, unsigned pre0,
+                          unsigned msk0) {
+    if (total <= 128) {
+      // exact rank of each candidate among the candidates
+      if ((int)threadIdx.x < total) {
+        const unsigned key = ck[threadIdx.x];
+        int gtc = 0, eqc = 0;
+        for (int y = 0; y < total; ++y) {
+          gtc += ck[y] > key;
+          eqc += ck[y] == key;
         }
-      {
-        int ab = 0;   // keys of this slice in bins above b*
-        for (int e = bstar + 1 + (int)threadIdx.x; e < kBins; e += blockDim.x) ab += (int)hist[0][e];
-        ab = warp_sum_int(ab);
-        if (lane == 0) scan_buf[warp] = ab;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-          int sum = 0;
-          for (int w = 0; w < nwarps; ++w) sum += scan_buf[w];
-          cl.map_shared_rank(above_r, 0)[rank] = sum;
+        if (gtc < kin && gtc + eqc >= kin) {   // several equal keys write the same values
+          sh_prefix = key;
+          sh_krem = kin - gtc;
         }
-      }
-      cl.sync();   // S3: rank 0 holds all `total` candidates and every CTA's count above
-      unsigned mine[2] = {0u, 0u};
-      unsigned char mrank[2] = {0, 0};
-#pragma unroll
-      for (int slot = 0; slot < 2; ++slot) {
-        const int x = (int)threadIdx.x + slot * (int)blockDim.x;
-        if (x < total) { mine[slot] = cand0[x]; mrank[slot] = crank0[x]; }
-      }
-      int ab_r = 0;
-      if (threadIdx.x < 16 && (int)threadIdx.x < CS) ab_r = cl.map_shared_rank(above_r, 0)[threadIdx.x];
-      cl.barrier_arrive();   // done reading rank 0; the matching wait is at the very end
-      fast_offsets = true;
-      __syncthreads();
-#pragma unroll
-      for (int slot = 0; slot < 2; ++slot) {
-        const int x = (int)threadIdx.x + slot * (int)blockDim.x;
-        if (x < total) { cand[x] = mine[slot]; cand_rank[x] = mrank[slot]; }
-      }
-      if (threadIdx.x < 16) gt_r[threadIdx.x] = ab_r;
-      __syncthreads();
-      if (total <= 128) {
-        // exact rank of each candidate among the candidates
-        if ((int)threadIdx.x < total) {
-          const unsigned key = cand[threadIdx.x];
-          int gtc = 0, eqc = 0;
-          for (int y = 0; y < total; ++y) {
-            gtc += cand[y] > key;
-            eqc += cand[y] == key;
-          }
-          if (gtc < kin && gtc + eqc >= kin) {   // several equal keys write the same values
-            sh_prefix = key;
-            sh_krem = kin - gtc;
-          }
-        }
-        __syncthreads();
-        prefix = sh_prefix;
-        krem = sh_krem;
-      } else {
-        // three radix passes over the candidates, inside this CTA (no cluster barrier)
-        unsigned pre = 0, msk = 0;
-        int kr = kin;
-        const int shifts[3] = {21, 10, 0};
-        const int widths[3] = {11, 11, 10};
-        for (int pass = 0; pass < 3; ++pass) {
-          const int shift = shifts[pass];
-          const unsigned dmask = (1u << widths[pass]) - 1u;
-          for (int e = threadIdx.x; e < kBins; e += blockDim.x) hist[0][e] = 0;
-          __syncthreads();
-          for (int x = threadIdx.x; x < total; x += blockDim.x) {
-            const unsigned key = cand[x];
-            if ((key & msk) == pre) atomicAdd(&hist[0][(key >> shift) & dmask], 1u);
-          }
-          __syncthreads();
-          const int b0 = kBins - 1 - 2 * (int)threadIdx.x, b1 = b0 - 1;
-          const unsigned c0 = hist[0][b0], c1 = hist[0][b1];
-          int tot2;
-          const int above2 = block_exclusive_scan((int)(c0 + c1), scan_buf, tot2);
-          if (above2 < kr && above2 + (int)(c0 + c1) >= kr) {
-            const bool first = above2 + (int)c0 >= kr;
-            sh_prefix = pre | ((unsigned)(first ? b0 : b1) << shift);
-            sh_krem = kr - (first ? above2 : above2 + (int)c0);
-          }
-          __syncthreads();
-          pre = sh_prefix;
-          kr = sh_krem;
-          msk |= dmask << shift;
-        }
-        prefix = pre;
-        krem = kr;
-      }
-      // per rank: keys > T (above the bin, or candidates above T) and keys == T
-      for (int x = threadIdx.x; x < total; x += blockDim.x) {
-        if (cand[x] > prefix) atomicAdd(&gt_r[cand_rank[x]], 1);
-        else if (cand[x] == prefix) atomicAdd(&eq_r[cand_rank[x]], 1);
       }
       __syncthreads();
+      prefix = sh_prefix;
+      krem = sh_krem;
     } else {
-      need_radix = true;
+      // three radix passes over the candidates, inside this CTA (no cluster barrier)
+      unsigned pre = pre0, msk = msk0;
+      int kr = kin;
+      // 11-bit digits from the top of the bits not yet fixed (the last digit may be shorter)
+      const int free_bits = 32 - __popc(msk0);
+      for (int hi = free_bits; hi > 0; hi -= 11) {
+        const int width = hi < 11 ? hi : 11, shift = hi - width;
+        const unsigned dmask = (1u << width) - 1u;
+        for (int e = threadIdx.x; e < kBins; e += blockDim.x) hist[0][e] = 0;
+        __syncthreads();
+        for (int x = threadIdx.x; x < total; x += blockDim.x) {
+          const unsigned key = ck[x];
+          if ((key & msk) == pre) atomicAdd(&hist[0][(key >> shift) & dmask], 1u);
+        }
+        __syncthreads();
+        const int b0 = kBins - 1 - 2 * (int)threadIdx.x, b1 = b0 - 1;
+        const unsigned c0 = hist[0][b0], c1 = hist[0][b1];
+        int tot2;
+        const int above2 = block_exclusive_scan((int)(c0 + c1), scan_buf, tot2);
+        if (above2 < kr && above2 + (int)(c0 + c1) >= kr) {
+          const bool first = above2 + (int)c0 >= kr;
+          sh_prefix = pre | ((unsigned)(first ? b0 : b1) << shift);
+          sh_krem = kr - (first ? above2 : above2 + (int)c0);
+        }
+        __syncthreads();
+        pre = sh_prefix;
+        kr = sh_krem;
+        msk |= dmask << shift;
+      }
+      prefix = pre;
+      krem = kr;
+    }
+    // per rank: keys > T (above the bin, or candidates above T) and keys == T
+    for (int x = threadIdx.x; x < total; x += blockDim.x) {
+      if (ck[x] > prefix) atomicAdd(&gt_r[cr[x]], 1);
+      else if (ck[x] == prefix) atomicAdd(&eq_r[cr[x]], 1);
+    }
+    __syncthreads();
+  };
+  if (fast) {
+    // ---- the threshold prefix bin b* and the count above it come from the indexer's
+    //      histogram.  Each CTA lists its own keys in b* and counts its keys above b*;
+    //      after one cluster barrier every CTA gathers all lists.  A histogram that
+    //      does not match the keys (lists or counts differ from it) falls back to the
+    //      radix passes, so a stale histogram costs time, never correctness.
+    const unsigned bstar = (unsigned)sh_bin;
+    const int kin = k - sh_above, total = sh_incount;
+    bool ok = total <= kCandMax;   // uniform
+    if (ok) {
+      // warp runs as in the output passes below: each warp lists the slice positions of
+      // its keys in or above b* (in index order, in kbin, which the fast path does not
+      // otherwise use) and counts the keys above b*; keys in b* also go to this CTA's
+      // candidate list
+      int ab = 0;
+      for (int j0 = w0; j0 < w1; j0 += 32) {
+        const int j = j0 + lane;
+        const unsigned key = j < w1 ? keys[j] : 0u, pre = key >> (32 - kPrefixBits);
+        const bool isa = j < w1 && pre > bstar, isc = j < w1 && pre == bstar;
+        const unsigned ba = __ballot_sync(0xffffffffu, isa), bs = ba | __ballot_sync(0xffffffffu, isc);
+        if (isa || isc) kbin[w0 + nsel + __popc(bs & lt)] = (unsigned short)j;
+        if (isc) {
+          const int slot = atomicAdd(&sh_cand, 1);
+          if (slot < kCandMax) cand[slot] = key;
+        }
+        nsel += __popc(bs);
+        ab += __popc(ba);
+      }
+      if (lane == 0) scan_buf[warp] = ab;
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        int sum = 0;
+        for (int w = 0; w < nwarps; ++w) sum += scan_buf[w];
+        sh_myab = sum;
+      }
+      cl.sync();   // S3: every CTA's list and count above b* are final
+      // every CTA has read the row's prefix histogram: leave it zeroed for the next call
+      for (int e = rank * (kPrefixBins / CS) + (int)threadIdx.x; e < (rank + 1) * (kPrefixBins / CS); e += blockDim.x)
+        ghist[(long long)row * kPrefixBins + e] = 0u;
+      if (threadIdx.x < 16) {
+        const int r = (int)threadIdx.x;
+        above_r[r] = r < CS ? *cl.map_shared_rank(&sh_cand, r) : 0;   // list lengths
+        gt_r[r] = r < CS ? *cl.map_shared_rank(&sh_myab, r) : 0;      // keys above b*
+      }
+      __syncthreads();
+      long long lsum = 0, asum = 0;
+      for (int r = 0; r < CS; ++r) { lsum += above_r[r]; asum += gt_r[r]; }
+      ok = lsum == total && asum == sh_above;   // the same in every CTA
+      if (ok) {
+        // every candidate is fetched by one thread (all remote loads in flight at once)
+        static_assert(2 * kBins >= kCandMax && 4 * kBins >= kCandMax, "gather arrays fit in hist[1..3]");
+        unsigned *allc = &hist[1][0];                                           // [kCandMax] gathered keys
+        unsigned char *allr = reinterpret_cast<unsigned char *>(&hist[3][0]);   // ... and their ranks
+        int offs[17];
+        offs[0] = 0;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) offs[r + 1] = offs[r] + above_r[r];
+        for (int x = threadIdx.x; x < total; x += blockDim.x) {
+          int r = 0;
+#pragma unroll
+          for (int q = 1; q < 16; ++q) r += x >= offs[q] ? 1 : 0;
+          int base_r = 0;
+#pragma unroll
+          for (int q = 0; q < 16; ++q) base_r = q == r ? offs[q] : base_r;
+          allc[x] = cl.map_shared_rank(cand, r)[x - base_r];
+          allr[x] = (unsigned char)r;
+        }
+        cl.barrier_arrive();   // done reading peers' lists; the matching wait is at the very end
+        fast_offsets = true;
+        fast_list = true;
+        __syncthreads();
+        select_among(allc, allr, total, kin, bstar << (32 - kPrefixBits), ~0u << (32 - kPrefixBits));
+      }
+    } else {
+      cl.sync();   // every CTA has read the row's prefix histogram
+      for (int e = rank * (kPrefixBins / CS) + (int)threadIdx.x; e < (rank + 1) * (kPrefixBins / CS); e += blockDim.x)
+        ghist[(long long)row * kPrefixBins + e] = 0u;
+    }
+    need_radix = !ok;
+  } else {
+    cl.sync();   // S1: every CTA's (min, max) visible; every part[] / counter zeroed
+    if (ghist) {   // every CTA has read the row's prefix histogram: leave it zeroed for the next call
+      for (int e = rank * (kPrefixBins / CS) + (int)threadIdx.x; e < (rank + 1) * (kPrefixBins / CS); e += blockDim.x)
+        ghist[(long long)row * kPrefixBins + e] = 0u;
+    }
+    unsigned gmin = 0xFFFFFFFFu, gmax = 0u;
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      if (r < CS) {
+        const unsigned *mm = cl.map_shared_rank(sh_minmax, r);
+        gmin = min(gmin, mm[0]);
+        gmax = max(gmax, mm[1]);
+      }
+    }
+    const float vmin = key_float(gmin), vmax = key_float(gmax);
+    const float scale = (float)kBins / (vmax - vmin);
+    const bool binned = gmax > gmin && isfinite(scale) && scale > 0.f && isfinite(vmin) && isfinite(vmax);
+    need_radix = !binned;
+    if (binned) {
+      // ---- value histogram (bin(v) is monotone in v); non-empty bins are added
+      //      straight into the owner CTA's merged array
+      const int per = kBins / CS;
+      unsigned *hsub = hist[warp & 3];
+      for (int j = threadIdx.x; j < len; j += blockDim.x) {
+        const int bin = min(kBins - 1, (int)((key_float(keys[j]) - vmin) * scale));
+        kbin[j] = (unsigned short)bin;
+        atomicAdd(&hsub[bin], 1u);
+      }
+      __syncthreads();
+      for (int e = threadIdx.x; e < kBins; e += blockDim.x) {
+        const unsigned v = hist[0][e] + hist[1][e] + hist[2][e] + hist[3][e];
+        hist[0][e] = v;
+        if (v) atomicAdd(cl.map_shared_rank(part, e / per) + e, v);
+      }
+      cl.sync();   // S2: merged histogram complete
+      // thread x owns bins 2047-2x and 2046-2x (descending)
+      const int b0 = kBins - 1 - 2 * (int)threadIdx.x, b1 = b0 - 1;
+      const unsigned c0 = cl.map_shared_rank(part, b0 / per)[b0];
+      const unsigned c1 = cl.map_shared_rank(part, b1 / per)[b1];
+      int tot;
+      const int above = block_exclusive_scan((int)(c0 + c1), scan_buf, tot);   // keys in higher bins
+      if (above < k && above + (int)(c0 + c1) >= k) {
+        const bool first = above + (int)c0 >= k;
+        sh_bin = first ? b0 : b1;
+        sh_above = first ? above : above + (int)c0;
+        sh_incount = (int)(first ? c0 : c1);
+      }
+      __syncthreads();
+      const int bstar = sh_bin, kin = k - sh_above, total = sh_incount;
+      if (total <= kCandMax) {
+        // ---- the threshold bin's keys of every CTA (with their rank) and every CTA's
+        //      count of keys above the bin go to rank 0
+        unsigned *cand0 = cl.map_shared_rank(cand, 0);
+        unsigned char *crank0 = cl.map_shared_rank(cand_rank, 0);
+        int *cnt0 = cl.map_shared_rank(&sh_cand, 0);
+        for (int j = threadIdx.x; j < len; j += blockDim.x)
+          if (kbin[j] == bstar) {
+            const int slot = atomicAdd(cnt0, 1);
+            cand0[slot] = keys[j];
+            crank0[slot] = (unsigned char)rank;
+          }
+        {
+          int ab = 0;   // keys of this slice in bins above b*
+          for (int e = bstar + 1 + (int)threadIdx.x; e < kBins; e += blockDim.x) ab += (int)hist[0][e];
+          ab = warp_sum_int(ab);
+          if (lane == 0) scan_buf[warp] = ab;
+          __syncthreads();
+          if (threadIdx.x == 0) {
+            int sum = 0;
+            for (int w = 0; w < nwarps; ++w) sum += scan_buf[w];
+            cl.map_shared_rank(above_r, 0)[rank] = sum;
+          }
+        }
+        cl.sync();   // S3: rank 0 holds all `total` candidates and every CTA's count above
+        constexpr int kSlots = kCandMax / kTopkThreads;
+        unsigned mine[kSlots];
+        unsigned char mrank[kSlots];
+#pragma unroll
+        for (int slot = 0; slot < kSlots; ++slot) {
+          const int x = (int)threadIdx.x + slot * (int)blockDim.x;
+          mine[slot] = x < total ? cand0[x] : 0u;
+          mrank[slot] = x < total ? crank0[x] : (unsigned char)0;
+        }
+        int ab_r = 0;
+        if (threadIdx.x < 16 && (int)threadIdx.x < CS) ab_r = cl.map_shared_rank(above_r, 0)[threadIdx.x];
+        cl.barrier_arrive();   // done reading rank 0; the matching wait is at the very end
+        fast_offsets = true;
+        __syncthreads();
+#pragma unroll
+        for (int slot = 0; slot < kSlots; ++slot) {
+          const int x = (int)threadIdx.x + slot * (int)blockDim.x;
+          if (x < total) { cand[x] = mine[slot]; cand_rank[x] = mrank[slot]; }
+        }
+        if (threadIdx.x < 16) gt_r[threadIdx.x] = ab_r;
+        __syncthreads();
+        select_among(cand, cand_rank, total, kin, 0u, 0u);
+      } else {
+        need_radix = true;
+      }
     }
   }
   if (need_radix) {
@@ -437,25 +568,36 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_cluster(CacheView c, int 
     }
   }
   // prefix = T, the k-th largest key; krem keys equal to T are still to be taken.
-  // Warp w owns the contiguous run [w*seg, (w+1)*seg) of this slice and walks it
-  // once, 32 keys at a time (coalesced, conflict-free): it counts the keys > T and
-  // == T and compacts their slice positions, in index order, to the front of its
-  // own run (in place: a round writes only below the keys it has read; bit 31
-  // marks a key == T).  One block scan orders the warps; the output pass then walks
-  // only the compacted lists.
-  const unsigned lt = (1u << lane) - 1u;
-  const int seg = ((len + nwarps - 1) / nwarps + 31) & ~31;
-  const int w0 = min(len, warp * seg), w1 = min(len, w0 + seg);
+  // Each warp counts its keys > T and == T and compacts their slice positions, in
+  // index order, to the front of its own run of keys[] (in place: a round writes
+  // only below the keys it has still to read; bit 31 marks a key == T).  It walks
+  // either its whole run or, on the fast path, only its list of keys in or above the
+  // threshold bin.  One block scan orders the warps; the output pass walks the
+  // compacted lists.
   int gw = 0, ew = 0;   // this warp's counts of keys > T and == T
-  for (int j0 = w0; j0 < w1; j0 += 32) {
-    const int j = j0 + lane;
-    const unsigned key = j < w1 ? keys[j] : 0u;
-    const bool isg = j < w1 && key > prefix, ise = j < w1 && key == prefix;
-    const unsigned bg = __ballot_sync(0xffffffffu, isg), be = __ballot_sync(0xffffffffu, ise);
-    const unsigned bs = bg | be;
-    if (isg || ise) keys[w0 + gw + ew + __popc(bs & lt)] = (unsigned)j | (ise ? 0x80000000u : 0u);
-    gw += __popc(bg);
-    ew += __popc(be);
+  if (fast_list) {
+    for (int i0 = 0; i0 < nsel; i0 += 32) {
+      const int i = i0 + lane;
+      const int j = i < nsel ? (int)kbin[w0 + i] : 0;
+      const unsigned key = i < nsel ? keys[j] : 0u;
+      const bool isg = i < nsel && key > prefix, ise = i < nsel && key == prefix;
+      const unsigned bg = __ballot_sync(0xffffffffu, isg), be = __ballot_sync(0xffffffffu, ise);
+      const unsigned bs = bg | be;
+      if (isg || ise) keys[w0 + gw + ew + __popc(bs & lt)] = (unsigned)j | (ise ? 0x80000000u : 0u);
+      gw += __popc(bg);
+      ew += __popc(be);
+    }
+  } else {
+    for (int j0 = w0; j0 < w1; j0 += 32) {
+      const int j = j0 + lane;
+      const unsigned key = j < w1 ? keys[j] : 0u;
+      const bool isg = j < w1 && key > prefix, ise = j < w1 && key == prefix;
+      const unsigned bg = __ballot_sync(0xffffffffu, isg), be = __ballot_sync(0xffffffffu, ise);
+      const unsigned bs = bg | be;
+      if (isg || ise) keys[w0 + gw + ew + __popc(bs & lt)] = (unsigned)j | (ise ? 0x80000000u : 0u);
+      gw += __popc(bg);
+      ew += __popc(be);
+    }
   }
   int tot;
   const int ex = block_exclusive_scan(lane == 0 ? ((ew << 16) | gw) : 0, scan_buf, tot);   // counts < 2^16
@@ -506,9 +648,19 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_cluster(CacheView c, int 
 // Rows with few queries get a cluster of up to 16 CTAs each; many rows get one
 // CTA each.  Rows whose slice would not fit in shared memory use k_topk_row.
 cudaError_t launch_topk(const CacheView &c, int batch, int n_q, const float *scores, long long stride, int k,
-                        int32_t *out_idx, int32_t *out_count, int num_sms, cudaStream_t st) {
+                        int32_t *out_idx, int32_t *out_count, unsigned *hist, int num_sms, cudaStream_t st) {
   const int rows = batch * n_q;
   const long long n_cap = c.cap < stride ? c.cap : stride;
+  // the row kernel does not read the indexer's prefix histograms; they are left zeroed
+  // for the next call all the same
+  auto row_kernel = [&]() -> cudaError_t {
+    if (hist) {
+      const cudaError_t e = cudaMemsetAsync(hist, 0, (size_t)rows * kPrefixBins * sizeof(unsigned), st);
+      if (e != cudaSuccess) return e;
+    }
+    return launch_pdl(k_topk_row, dim3(rows), dim3(kTopkThreads), 0, st, 1, c, n_q, scores, stride, k, out_idx,
+                      out_count);
+  };
   int cs = 1;
   if (rows < num_sms) {
     cs = 16;
@@ -516,9 +668,7 @@ cudaError_t launch_topk(const CacheView &c, int batch, int n_q, const float *sco
   }
   const long long slice = (n_cap + cs - 1) / cs;
   const size_t smem = (size_t)slice * 6;   // uint32 key + uint16 bin per score
-  if (smem > 160 * 1024 || cs > 16 || kBins % cs)
-    return launch_pdl(k_topk_row, dim3(rows), dim3(kTopkThreads), 0, st, 1, c, n_q, scores, stride, k, out_idx,
-                      out_count);
+  if (smem > 160 * 1024 || cs > 16 || kBins % cs) return row_kernel();
   cudaError_t e = cudaFuncSetAttribute(k_topk_cluster, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
   if (e == cudaSuccess && cs > 8)
     e = cudaFuncSetAttribute(k_topk_cluster, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -527,12 +677,11 @@ cudaError_t launch_topk(const CacheView &c, int batch, int n_q, const float *sco
     const size_t sm = (size_t)((n_cap + cs - 1) / cs) * 6;
     if (sm > 160 * 1024) break;
     e = launch_pdl(k_topk_cluster, dim3(cs, rows), dim3(kTopkThreads), sm, st, cs, c, n_q, scores, stride, k, out_idx,
-                   out_count, (int)((n_cap + cs - 1) / cs));
+                   out_count, hist, (int)((n_cap + cs - 1) / cs));
     if (e == cudaSuccess || cs == 1) return e;
     cudaGetLastError();   // cluster too large for this device: halve it
   }
-  return launch_pdl(k_topk_row, dim3(rows), dim3(kTopkThreads), 0, st, 1, c, n_q, scores, stride, k, out_idx,
-                    out_count);
+  return row_kernel();
 }
 
 }  // namespace csa
