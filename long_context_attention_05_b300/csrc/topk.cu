@@ -186,6 +186,15 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_cluster(CacheView c, int 
   const long long lo = min(n, rank * L), hi = min(n, lo + L);
   const int len = (int)(hi - lo);
   const float *s = scores + (long long)row * stride + lo;
+  // the row's prefix counts (fast path, below) are loaded along with the scores
+  static_assert(kPrefixBins == 8 * kTopkThreads, "one thread per 8 prefix bins");
+  const int hb = kPrefixBins - 8 * ((int)threadIdx.x + 1);   // this thread's bins hb .. hb+7
+  uint4 h0 = make_uint4(0, 0, 0, 0), h1 = make_uint4(0, 0, 0, 0);
+  if (ghist != nullptr) {
+    const unsigned *hr = ghist + (long long)row * kPrefixBins;
+    h0 = *reinterpret_cast<const uint4 *>(hr + hb);
+    h1 = *reinterpret_cast<const uint4 *>(hr + hb + 4);
+  }
   // ---- load: 16-byte loads for the aligned middle, scalars for the ends; and the
   //      slice's min / max key
   unsigned kmin = 0xFFFFFFFFu, kmax = 0u;
@@ -243,10 +252,6 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_cluster(CacheView c, int 
   //      no histogram pass, no cluster exchange of histograms.
   bool fast = false;
   if (ghist != nullptr) {   // uniform
-    static_assert(kPrefixBins == 8 * kTopkThreads, "one thread per 8 prefix bins");
-    const unsigned *hr = ghist + (long long)row * kPrefixBins;
-    const int hb = kPrefixBins - 8 * ((int)threadIdx.x + 1);   // this thread's bins hb .. hb+7
-    const uint4 h0 = *reinterpret_cast<const uint4 *>(hr + hb), h1 = *reinterpret_cast<const uint4 *>(hr + hb + 4);
     const unsigned cb[8] = {h1.w, h1.z, h1.y, h1.x, h0.w, h0.z, h0.y, h0.x};   // descending bins
     int s8 = 0;
 #pragma unroll
@@ -353,18 +358,28 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_cluster(CacheView c, int 
       // otherwise use) and counts the keys above b*; keys in b* also go to this CTA's
       // candidate list
       int ab = 0;
-      for (int j0 = w0; j0 < w1; j0 += 32) {
-        const int j = j0 + lane;
-        const unsigned key = j < w1 ? keys[j] : 0u, pre = key >> (32 - kPrefixBits);
-        const bool isa = j < w1 && pre > bstar, isc = j < w1 && pre == bstar;
-        const unsigned ba = __ballot_sync(0xffffffffu, isa), bs = ba | __ballot_sync(0xffffffffu, isc);
-        if (isa || isc) kbin[w0 + nsel + __popc(bs & lt)] = (unsigned short)j;
-        if (isc) {
-          const int slot = atomicAdd(&sh_cand, 1);
-          if (slot < kCandMax) cand[slot] = key;
+      // four rounds per iteration, their shared-memory loads issued together
+      for (int j00 = w0; j00 < w1; j00 += 128) {
+        unsigned kq[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int j = j00 + 32 * q + lane;
+          kq[q] = j < w1 ? keys[j] : 0u;
         }
-        nsel += __popc(bs);
-        ab += __popc(ba);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int j = j00 + 32 * q + lane;
+          const unsigned key = kq[q], pre = key >> (32 - kPrefixBits);
+          const bool isa = j < w1 && pre > bstar, isc = j < w1 && pre == bstar;
+          const unsigned ba = __ballot_sync(0xffffffffu, isa), bs = ba | __ballot_sync(0xffffffffu, isc);
+          if (isa || isc) kbin[w0 + nsel + __popc(bs & lt)] = (unsigned short)j;
+          if (isc) {
+            const int slot = atomicAdd(&sh_cand, 1);
+            if (slot < kCandMax) cand[slot] = key;
+          }
+          nsel += __popc(bs);
+          ab += __popc(ba);
+        }
       }
       if (lane == 0) scan_buf[warp] = ab;
       __syncthreads();
