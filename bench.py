@@ -127,7 +127,8 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(sm), "source": self.backend}
 
 
-INDEXER_SOURCES = ("long_context_attention_05_b300/csrc/indexer_tc.cu", "long_context_attention_05_b300/csrc/common.cuh")
+INDEXER_SOURCES = ("long_context_attention_05_b300/csrc/indexer_tc.cu", "long_context_attention_05_b300/csrc/common.cuh",
+                   "long_context_attention_05_b300/csrc/kernels.h")
 INDEXER_PROFILE = "profiles/k_index_tc_csa_decode_1m.md"
 
 
