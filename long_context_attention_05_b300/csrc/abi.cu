@@ -186,6 +186,7 @@ csa_status attend_common(const csa_cache *c, int batch, int n_q, const void *q, 
   a.n_q = n_q; a.heads = heads; a.q_dtype = q_dtype; a.out_dtype = out_dtype;
   a.q = (const uint8_t *)q; a.sink = sink; a.idx = idx; a.k = k;
   a.n_splits = p.n_splits; a.chunks_per_split = p.cps;
+  a.keys_per_split = p.cps * (p.tc ? 64 : csa::kKC);
   a.part_o = need ? (float *)((char *)ws + kHeader) : nullptr;
   a.part_ml = need ? (float *)((char *)ws + kHeader + p.part_o_bytes) : nullptr;
   a.out = (uint8_t *)out; a.out_lse = out_lse;

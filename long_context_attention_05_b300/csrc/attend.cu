@@ -45,6 +45,9 @@ __global__ void __launch_bounds__(kAttThreads) k_attend(AttendArgs a) {
   const int nh = min(kHG, a.heads - h0);
   const int split = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // splits past this row's keys (the plan covers the key-list capacity) do nothing;
+  // the merge reads only the splits that hold keys
+  if (a.n_splits > 1 && (long long)split * a.keys_per_split >= U) return;   // uniform
 
   // query heads, rotated at t
   for (int e = tid; e < nh * d; e += blockDim.x)
@@ -199,10 +202,10 @@ __global__ void __launch_bounds__(kAttThreads) k_attend(AttendArgs a) {
 constexpr int kCombThreads = 512;
 constexpr int kCombHeads = 2;   // heads per CTA
 __global__ void __launch_bounds__(kCombThreads) k_attend_combine(AttendArgs a) {
-  extern __shared__ float wts[];   // [kCombHeads][n_splits]
+  extern __shared__ float wts[];   // [kCombHeads][n_splits] (the first S of each used)
   __shared__ float red[kCombHeads][2][kCombThreads / 32];
   const int row = blockIdx.y;
-  const int d = a.c.d, S = a.n_splits;
+  const int d = a.c.d;
   pdl_wait();
   pdl_trigger();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -212,12 +215,24 @@ __global__ void __launch_bounds__(kCombThreads) k_attend_combine(AttendArgs a) {
   const int hs = tid / TPH, t2 = tid % TPH;
   const int h = blockIdx.x * kCombHeads + hs;
   const bool hv = h < a.heads;
-  const long long base = (long long)row * S * a.heads + h;
+  const int SP = a.n_splits;   // stride of the partial arrays
+  const long long base = (long long)row * SP * a.heads + h;
+  // this thread's first split's (m, l) and the sink load together with n_tokens
   const float z = hv ? __ldg(a.sink + h) : 0.f;
+  const float2 ml0 = hv && t2 < SP ? *reinterpret_cast<const float2 *>(a.part_ml + (base + (long long)t2 * a.heads) * 2)
+                                  : make_float2(-INFINITY, 0.f);
+  // only the splits that hold keys of this row were written (the same count the
+  // attention kernel derives from n_tokens)
+  const int bq = row / a.n_q, iq = row % a.n_q;
+  const long long t = a.c.n_tokens[bq] - a.n_q + iq;
+  const long long U = (a.idx ? a.k : min((t + 1) / a.c.m, a.c.cap)) + a.c.n_win;
+  const int S = (int)max(0LL, min((long long)SP, (U + a.keys_per_split - 1) / a.keys_per_split));
   // per head: M and the split weights (the threads of a head are whole warps)
   float m = z;
-  if (hv)
-    for (int s = t2; s < S; s += TPH) m = fmaxf(m, a.part_ml[(base + (long long)s * a.heads) * 2]);
+  if (hv) {
+    if (t2 < S) m = fmaxf(m, ml0.x);
+    for (int s = t2 + TPH; s < S; s += TPH) m = fmaxf(m, a.part_ml[(base + (long long)s * a.heads) * 2]);
+  }
   m = warp_max(m);
   if (lane == 0) red[hs][0][warp % (NW / kCombHeads)] = m;
   __syncthreads();
@@ -225,13 +240,14 @@ __global__ void __launch_bounds__(kCombThreads) k_attend_combine(AttendArgs a) {
 #pragma unroll
   for (int i = 1; i < NW / kCombHeads; ++i) M = fmaxf(M, red[hs][0][i]);
   float lp = 0.f;
-  if (hv)
+  if (hv) {
     for (int s = t2; s < S; s += TPH) {
-      const float ms = a.part_ml[(base + (long long)s * a.heads) * 2];
-      const float ws = ms > -INFINITY ? expf(ms - M) : 0.f;
+      const float2 ml = s == t2 ? ml0 : *reinterpret_cast<const float2 *>(a.part_ml + (base + (long long)s * a.heads) * 2);
+      const float ws = ml.x > -INFINITY ? expf(ml.x - M) : 0.f;
       wts[hs * S + s] = ws;
-      lp = fmaf(ws, a.part_ml[(base + (long long)s * a.heads) * 2 + 1], lp);
+      lp = fmaf(ws, ml.y, lp);
     }
+  }
   lp = warp_sum(lp);
   if (lane == 0) red[hs][1][warp % (NW / kCombHeads)] = lp;
   __syncthreads();

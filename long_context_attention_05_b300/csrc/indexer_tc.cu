@@ -165,9 +165,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
 
   const CacheView &c = a.c;
   // ---- work assignment.  Many query rows (>= one per SM): CTA y takes row y.
-  // Few rows: the grid is flat (one CTA per SM) and row r gets
-  // max(1, floor((SMs - rows) * tiles_r / T)) CTAs (T = all rows' tiles), so ragged
-  // context lengths stay balanced; every CTA derives the same partition from n_tokens.
+  // Few rows: the grid is flat (one CTA per SM) and row r gets ceil(tiles_r / L) CTAs
+  // for the smallest per-CTA tile load L that fits the grid, so ragged context lengths
+  // stay balanced; every CTA derives the same partition from n_tokens.
   __shared__ int sh_row, sh_sub, sh_cnt;
   __shared__ long long sh_nvis;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -214,13 +214,36 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) T += __shfl_xor_sync(0xffffffffu, T, o);
+    // Row r gets ceil(tiles_r / L) CTAs for the smallest tile load L that fits the
+    // grid: L lies in [ceil(T/G), ceil(T/(G-rows))] (the upper end always fits,
+    // since sum ceil(t/L) <= T/L + rows), found by bisection; equal rows settle at
+    // the lower end on the first probe.
+    const long long G = a.grid_sms;
+    auto ctas_needed = [&](long long L) -> long long {
+      long long need = 0;
+#pragma unroll
+      for (int u = 0; u < kMaxFlatRows / 32; ++u) {
+        if (u >= n_chunks) break;   // warp-uniform
+        need += (tiles[u] + L - 1) / L;
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) need += __shfl_xor_sync(0xffffffffu, need, o);
+      return need;
+    };
+    long long Llo = max(1LL, (T + G - 1) / G), Lhi = max(Llo, (T + (G - rows) - 1) / max(G - rows, 1LL));
+    if (ctas_needed(Llo) <= G) Lhi = Llo;
+    while (Llo < Lhi) {   // warp-uniform
+      const long long mid = (Llo + Lhi) >> 1;
+      if (ctas_needed(mid) <= G) Lhi = mid; else Llo = mid + 1;
+    }
+    const long long L = Lhi;
     int found_row = -1, found_sub = 0, found_cnt = 0, base = 0;
     long long found_nv = 0;
 #pragma unroll
     for (int u = 0; u < kMaxFlatRows / 32; ++u) {
       if (u >= n_chunks) break;   // warp-uniform
       const int r = lane + 32 * u;
-      const int cr = tiles[u] > 0 ? max(1, (int)((long long)(a.grid_sms - a.rows) * tiles[u] / max(T, 1LL))) : 0;
+      const int cr = (int)((tiles[u] + L - 1) / L);
       int incl = cr;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -339,31 +362,52 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
 
   if (warp == 0) {
     asm volatile("bar.sync 2, %0;" ::"n"(kThreads) : "memory");   // query loads are in flight
-    if (lane == 0) {   // ---- TMA producer
+    {   // ---- TMA producer: lane 0 issues; for paged caches the whole warp keeps the
+        //      page ids of the next 32 logical pages in flight (lane l holds page
+        //      base + l), so no copy waits on a page-table load
       const uint64_t policy = l2_evict_first_policy();
       int issued = 0;
+      const int *ptab = c.page_size ? c.page_table + (long long)b * c.max_pages : nullptr;
+      auto page_chunk = [&](long long base) -> int {   // page id of logical page base + lane
+        const long long lp = base + lane;
+        return (ptab && lp < c.max_pages) ? __ldg(ptab + lp) : 0;
+      };
+      long long pbase = -1;
+      int pcur = 0, pnext = 0;
       for (int it = 0; it < n_it; ++it) {
         const int s = it % kStages;
         const uint32_t ph = (uint32_t)(it / kStages) & 1u;
-        if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, a.status)) break;
-        mbar_expect_tx(&full[s], kStageBytes);
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait(&empty[s], ph ^ 1u, abort_flag, a.status);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;   // warp-uniform
+        if (lane == 0) mbar_expect_tx(&full[s], kStageBytes);
         const long long tile = tile_lo + it;
         if (c.page_size == 0) {
-          tma_load_2d(stage + s * kStageBytes, &kmap, &full[s], 0, (int)((long long)b * c.max_entries + tile * kTileM),
-                      policy);
+          if (lane == 0)
+            tma_load_2d(stage + s * kStageBytes, &kmap, &full[s], 0, (int)((long long)b * c.max_entries + tile * kTileM),
+                        policy);
         } else {
           for (int r0 = 0; r0 < kTileM; r0 += a.box_rows) {
             const long long j0 = tile * kTileM + r0;
-            long long lp = j0 / c.page_size;
-            if (lp >= c.max_pages) lp = 0;   // past the table: any valid page (never scored)
-            const long long pg = __ldg(c.page_table + (long long)b * c.max_pages + lp);
-            tma_load_2d(stage + s * kStageBytes + r0 * kDI, &kmap, &full[s], 0,
-                        (int)(pg * c.page_size + j0 % c.page_size), policy);
+            const long long lp = j0 / c.page_size;   // past the table: page id 0 (never scored)
+            if (pbase < 0 || lp >= pbase + 64) {     // (re)start: this chunk and the next
+              pbase = lp;
+              pcur = page_chunk(pbase);
+              pnext = page_chunk(pbase + 32);
+            } else if (lp >= pbase + 32) {            // next chunk: its ids are here, fetch the one after
+              pbase += 32;
+              pcur = pnext;
+              pnext = page_chunk(pbase + 32);
+            }
+            const int pg = __shfl_sync(0xffffffffu, pcur, (int)(lp - pbase));
+            if (lane == 0)
+              tma_load_2d(stage + s * kStageBytes + r0 * kDI, &kmap, &full[s], 0,
+                          (int)((long long)pg * c.page_size + j0 % c.page_size), policy);
           }
         }
         ++issued;
       }
-      if (*abort_flag) {   // let copies already issued land before shared memory goes away
+      if (lane == 0 && *abort_flag) {   // let copies already issued land before shared memory goes away
         for (int it = issued > kStages ? issued - kStages : 0; it < issued; ++it)
           for (int i = 0; i < (1 << 20) && !mbar_try_wait(&full[it % kStages], (uint32_t)(it / kStages) & 1u); ++i) {
           }
@@ -400,15 +444,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
     const int grp = (warp - 2) >> 2;   // epilogue group: tiles it with it % n_grp == grp
     // key scales are read four of this group's tiles ahead so their memory
     // latency overlaps the tiles in between instead of stalling each epilogue
-    auto scale_of = [&](int it2) -> float {
+    // paged caches: the page id of an entry is loaded one prefetch rotation before its
+    // scale, so neither load waits on the other inside a tile's epilogue
+    auto page_of = [&](int it2) -> int {
       const long long j2 = (tile_lo + it2) * kTileM + g * 32 + lane;
-      return (it2 < n_it && j2 < n_vis) ? __ldg(c.idx_scale + entry_row(c, b, j2)) : 0.f;
+      return (c.page_size && it2 < n_it && j2 < n_vis)
+                 ? __ldg(c.page_table + (long long)b * c.max_pages + j2 / c.page_size) : 0;
     };
-    // slot u of sc[] holds the scale of this group's tile it0 + n_grp*u; it is refilled
-    // in place four tiles ahead (no register shuffling that would wait on loads)
+    auto scale_of = [&](int it2, int pg) -> float {
+      const long long j2 = (tile_lo + it2) * kTileM + g * 32 + lane;
+      if (!(it2 < n_it && j2 < n_vis)) return 0.f;
+      const long long r = c.page_size ? (long long)pg * c.page_size + j2 % c.page_size : (long long)b * c.max_entries + j2;
+      return __ldg(c.idx_scale + r);
+    };
+    // slot u of sc[] holds the scale of this group's tile it0 + n_grp*u (pgn[u]: the page
+    // id for the tile four group-tiles later); both are refilled in place
     float sc[4];
+    int pgn[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) sc[u] = scale_of(grp + n_grp * u);
+    for (int u = 0; u < 4; ++u) pgn[u] = page_of(grp + n_grp * u);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      sc[u] = scale_of(grp + n_grp * u, pgn[u]);
+      pgn[u] = page_of(grp + n_grp * (u + 4));
+    }
     bool live = true;
     if (grp >= n_grp) live = false;
     for (int it0 = grp; it0 < n_it && live; it0 += 4 * n_grp) {
@@ -452,7 +511,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
           a.scores[(long long)row * a.stride + j] = v;
           if (a.hist) atomicAdd(&shist[float_key(v) >> (32 - kPrefixBits)], 1u);
         }
-        sc[u] = scale_of(it + 4 * n_grp);
+        sc[u] = scale_of(it + 4 * n_grp, pgn[u]);
+        pgn[u] = page_of(it + 8 * n_grp);
       }
     }
   }
@@ -534,8 +594,8 @@ cudaError_t launch_index_tc(const CacheView &c, int batch, int n_q, const void *
   if (rows_q >= num_sms || rows_q > kMaxFlatRows) {   // a row per CTA
     a.ctas_per_row = 1;
     grid = dim3(1, rows_q);
-  } else {                   // flat grid, CTAs split over rows by their tile counts: at most
-    a.ctas_per_row = 0;       // (SMs - rows) * share + 1 per row, i.e. <= SMs in all
+  } else {                   // flat grid, CTAs split over rows by their tile counts
+    a.ctas_per_row = 0;       // (ceil(tiles / L) per row, <= SMs in all)
     grid = dim3(num_sms, 1);
   }
   const size_t smem = index_tc_smem_bytes();

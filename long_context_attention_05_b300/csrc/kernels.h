@@ -69,6 +69,7 @@ struct AttendArgs {
   const int32_t *idx;   // nullptr: dense (HCA)
   int k;
   int n_splits, chunks_per_split;
+  int keys_per_split;   // chunks_per_split x the running kernel's keys per chunk
   float *part_o, *part_ml;
   uint8_t *out;
   float *out_lse;

@@ -676,10 +676,13 @@ cudaError_t launch_topk(const CacheView &c, int batch, int n_q, const float *sco
     return launch_pdl(k_topk_row, dim3(rows), dim3(kTopkThreads), 0, st, 1, c, n_q, scores, stride, k, out_idx,
                       out_count);
   };
+  // cluster size: up to 16 CTAs per row for few rows; with many rows, halve it while
+  // the grid exceeds two waves and the halved slices still fit in shared memory
+  constexpr long long kSliceMax = 160 * 1024 / 6;   // uint32 key + uint16 bin per score
   int cs = 1;
   if (rows < num_sms) {
     cs = 16;
-    while (cs > 1 && (long long)rows * cs > 2LL * num_sms && (n_cap + cs / 2 - 1) / (cs / 2) <= 32768) cs /= 2;
+    while (cs > 1 && (long long)rows * cs > 2LL * num_sms && (n_cap + cs / 2 - 1) / (cs / 2) <= kSliceMax) cs /= 2;
   }
   const long long slice = (n_cap + cs - 1) / cs;
   const size_t smem = (size_t)slice * 6;   // uint32 key + uint16 bin per score
