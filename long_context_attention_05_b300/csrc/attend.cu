@@ -47,7 +47,7 @@ __global__ void __launch_bounds__(kAttThreads) k_attend(AttendArgs a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // splits past this row's keys (the plan covers the key-list capacity) do nothing;
   // the merge reads only the splits that hold keys
-  if (a.n_splits > 1 && (long long)split * a.keys_per_split >= U) return;   // uniform
+  if (a.idx == nullptr && a.n_splits > 1 && (long long)split * a.keys_per_split >= U) return;   // uniform (dense rows)
 
   // query heads, rotated at t
   for (int e = tid; e < nh * d; e += blockDim.x)

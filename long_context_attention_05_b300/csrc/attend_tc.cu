@@ -93,8 +93,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttendArgs a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = warp & 3, qq = warp >> 2;
   // splits past this row's keys (the plan covers the key-list capacity) do nothing;
-  // the merge reads only the splits that hold keys
-  if (a.n_splits > 1 && (long long)split * a.keys_per_split >= U) return;   // uniform
+  // the merge reads only the splits that hold keys.  Only a dense (HCA) row can end
+  // early: a selected list always has k slots, so a sparse row's check needs no
+  // n_tokens and does not hold back the query loads below.
+  if (a.idx == nullptr && a.n_splits > 1 && (long long)split * a.keys_per_split >= U) return;   // uniform
 
   // key source of slot tid of a chunk: entry row (>= 0), -2 - ring row (window
   // token; the ring slot is resolved here, once per key, not per gathered piece)
