@@ -96,3 +96,40 @@ def test_invalid_call_arguments_rejected():
     assert lib.hca_attend(s, 1, 200, 1 << 20, L.CSA_BF16, 64, 1 << 20, 1 << 20, L.CSA_BF16, None, 1 << 20, big,
                           None) == 1
     assert lib.csa_device_status(None, None, None) == 1
+
+
+def _align256(n):
+    return (n + 255) // 256 * 256
+
+
+def _expected_workspace(batch, n_q, heads, k, d=512, n_win=128, entry_cap=1000):
+    """The workspace layout written out: a 256-byte header; from it, the scores of the
+    indexer (rows x entry capacity) or the attention's split partials, whichever is
+    larger; then, for decode-sized calls (rows <= 256) with a top-k, per-row
+    histograms of 8192 score-key prefixes at the end."""
+    rows = batch * n_q
+    chunks = -(-(k + n_win) // 64)              # tensor-core attention: 64-key chunks
+    splits = chunks if n_q == 1 else 1          # decode: one chunk per split
+    parts = rows * splits * heads
+    part_bytes = (_align256(parts * d * 4) + _align256(parts * 2 * 4)) if splits > 1 else 0
+    need = max(256 + _align256(rows * entry_cap * 4), 256 + part_bytes)
+    return _align256(need) + (rows * 8192 * 4 if rows <= 256 else 0)
+
+
+@pytest.mark.parametrize("batch,n_q", [(4, 1), (32, 1), (256, 1), (257, 1), (2, 300)])
+def test_workspace_layout_reserves_prefix_histograms_for_decode_sized_calls(batch, n_q):
+    lib = L.lib()
+    s = _struct()
+    got = lib.csa_workspace_size(ctypes.byref(s), batch, n_q, 64, 2048)
+    assert got == _expected_workspace(batch, n_q, 64, 2048)
+
+
+def test_split_plan_does_not_depend_on_the_batch():
+    """The attention's split count per row depends only on the key-list capacity, so
+    a row's reduction order (and its bits) cannot change with the rest of the batch:
+    the partials grow exactly linearly with the batch."""
+    lib = L.lib()
+    s = _struct(max_entries=10)   # tiny scores: the partials set the size
+    sizes = [lib.csa_workspace_size(ctypes.byref(s), b, 1, 64, 2048) - b * 8192 * 4 for b in (1, 2, 3, 8)]
+    per_row = [(sizes[i] - 256) for i in range(4)]
+    assert all(abs(per_row[i] / (1, 2, 3, 8)[i] - per_row[0]) < 512 for i in range(4))
