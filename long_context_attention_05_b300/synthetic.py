@@ -95,6 +95,10 @@ class Workload:
     extra_entries: int = 64     # spare entry capacity per sequence for repeated steps
     spare_pages: int = 0        # spare physical pages in the pool (paged caches)
 
+    def __post_init__(self):
+        if len(self.ctx) != self.batch:
+            raise ValueError(f"{self.name}: {len(self.ctx)} context lengths for batch {self.batch}")
+
     @property
     def n_entries(self):
         return tuple(c // self.m for c in self.ctx)
