@@ -400,7 +400,10 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_cluster(CacheView c, int 
       __syncthreads();
       long long lsum = 0, asum = 0;
       for (int r = 0; r < CS; ++r) { lsum += above_r[r]; asum += gt_r[r]; }
-      ok = lsum == total && asum == sh_above;   // the same in every CTA
+      // the lists and counts come from the keys themselves: b* is the threshold bin iff
+      // fewer than k keys lie above it and at least k lie in or above it (this holds
+      // whatever the histogram held)
+      ok = lsum == total && asum == sh_above && asum < k && asum + lsum >= k;   // the same in every CTA
       if (ok) {
         // every candidate is fetched by one thread (all remote loads in flight at once)
         static_assert(2 * kBins >= kCandMax && 4 * kBins >= kCandMax, "gather arrays fit in hist[1..3]");
