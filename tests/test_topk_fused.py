@@ -123,3 +123,15 @@ def test_fused_crowded_threshold_bin(kind):
             assert sorted(ref[0][b, 0].tolist()) == list(range(w.k))
     for rep in range(2):
         _same(_fused(w, cache, gi, ws), ref, f"{kind} call {rep}")
+
+
+@pytest.mark.parametrize("n_new", [64, 200])
+def test_fused_prefill_shaped_rows(n_new):
+    """Many query rows on one sequence: 64 rows take the flat indexer grid and 4-CTA
+    clusters, 200 rows (more than the SMs) one indexer CTA per row and single-CTA
+    clusters; both fill and consume the prefix histograms."""
+    w = S.config3(ctx=(8192,), n_new=n_new, k=256)
+    cache, gi, ws = _setup(w)
+    ref = _separate(w, cache, gi, ws)
+    for rep in range(2):
+        _same(_fused(w, cache, gi, ws), ref, f"prefill rows {n_new} call {rep}")
