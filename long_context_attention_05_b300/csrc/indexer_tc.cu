@@ -30,6 +30,9 @@
 // timeout sets the workspace status word and all roles stop issuing work.
 // Each CTA scores a contiguous range of 128-entry tiles of one query row, so its
 // query operand is built once (see the work assignment at the top of the kernel).
+// Given per-row histograms (the fused index + top-k call), the epilogue also counts
+// every score by the top kPrefixBits bits of its order-preserving key, in shared
+// memory, and adds the counts to the row's histogram at the end.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 

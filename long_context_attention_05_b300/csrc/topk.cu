@@ -136,6 +136,11 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_row(CacheView c, int n_q,
 // Bins that are too crowded (degenerate value ranges) fall back to three radix
 // passes over the ordered-integer keys.  Every decision is integer counting on
 // identical data in every CTA, so the result is deterministic.
+// With the indexer's per-row prefix histogram (fused call), steps 1-3 start from it:
+// every CTA finds the threshold prefix bin and the count above it by itself, lists
+// its keys in and above that bin, and one cluster barrier later gathers all CTAs'
+// keys of the bin; the histogram is checked against the keys and zeroed for the
+// next call.
 constexpr int kBins = 2048;
 constexpr int kCandMax = 4096;   // threshold-bin keys resolved without a pass over every key
 
