@@ -312,3 +312,121 @@ def test_cache_layout_is_about_two_percent_of_bf16_gqa8():
     gqa8 = 8 * 128 * 2 * 2                        # 8 kv heads x 128 dims x (K, V) x bf16
     ratio = per_layer / gqa8
     assert abs(ratio - figs["kv_cache_vs_bf16_gqa8"]["value"]) < 0.005, ratio
+
+
+# ----------------------------------------------------------------------------- window, paging, stored formats
+def test_window_positions_hand_values():
+    """The window of a query at t holds raw tokens max(0, t-W+1) .. t: the query's own
+    token included, W tokens once t >= W-1."""
+    assert O.window_positions(0, 128).tolist() == [0]
+    assert O.window_positions(5, 128).tolist() == [0, 1, 2, 3, 4, 5]
+    w = O.window_positions(200, 128)
+    assert w[0] == 73 and w[-1] == 200 and len(w) == 128 and np.all(np.diff(w) == 1)
+    assert O.window_positions(127, 128).tolist() == list(range(128))
+    assert O.window_positions(9, 1).tolist() == [9]
+    assert O.ring_slot(np.array([127, 128, 129, 300]), 128).tolist() == [127, 0, 1, 44]
+
+
+def test_entry_rows_contiguous_and_paged_hand_table():
+    # contiguous: sequence b owns rows [b*max_entries, (b+1)*max_entries)
+    assert O.entry_rows(3, 2, 10, None, 0).tolist() == [20, 21, 22]
+    # two pages of two entries per sequence, physical pages out of order
+    pt = np.array([[3, 1], [0, 2]], dtype=np.int32)
+    assert O.entry_rows(4, 0, 0, pt, 2).tolist() == [6, 7, 2, 3]
+    assert O.entry_rows(3, 1, 0, pt, 2).tolist() == [0, 1, 4]
+
+
+def test_decode_kv_scales_only_the_e4m3_dims_and_keeps_the_order():
+    nope = np.array([[0x38, 0x40], [0xB8, 0x00]], dtype=np.uint8)     # 1, 2 | -1, 0
+    scale = np.array([0.5, 4.0], dtype=np.float32)
+    rope = np.array([[0x3F80], [0xC000]], dtype=np.uint16)             # 1 | -2 (bf16)
+    got = O.decode_kv(nope, scale, rope, "e4m3")
+    assert got.tolist() == [[0.5, 1.0, 1.0], [-4.0, 0.0, -2.0]]
+    f = O.decode_kv(np.array([[1.5, -2.0]], np.float32), None, np.array([[7.0]], np.float32), "f32")
+    assert f.tolist() == [[1.5, -2.0, 7.0]]
+    k = O.decode_index_keys(np.array([[0x38, 0xC0]], np.uint8), np.array([0.25], np.float32), "e4m3")
+    assert k.tolist() == [[0.25, -0.5]]
+
+
+def test_e4m3_scale_subnormal_branch():
+    tiny = np.finfo(np.float32).tiny
+    assert O.e4m3_scale(np.array([1e-37, -3e-38])) == np.float32(1.0)    # amax/448 is subnormal
+    assert O.e4m3_scale(np.array([448 * tiny])) == np.float32(tiny)      # smallest normal scale is kept
+    assert O.e4m3_scale(np.array([0.0, -0.0])) == np.float32(1.0)
+    assert O.e4m3_scale(np.array([-896.0, 3.0])) == np.float32(2.0)      # |.| of a negative amax
+
+
+def test_compress_entries_e4m3_branch_hand_worked():
+    """Two blocks of m = 2 tokens, d = 6 (4 e4m3 dims + 2 rotary dims), equal gates:
+    each entry is the mean of its block.  Block 0 sits at position 0 (no turn); block
+    1 at position 2 (its single rotary pair turns by 2 radians)."""
+    x = np.array([[8, -2, 0, 6, 20, 0],
+                  [0, 0, 0, 0, 0, 2],
+                  [1, 1, 1, 1, 1, 0],
+                  [1, 1, 1, 1, 1, 0]], dtype=np.float64)
+    g = np.zeros_like(x)
+    out = O.compress_entries(x, g, np.zeros(2), 2, 2, 10000.0, "e4m3", 0, 2)
+    # block 0: mean nope [4, -1, 0, 3] -> scale fp32(4)/448 (the rotary dims [10, 1] do not
+    # enter the scale); codes 448 -> 0x7E, -112 -> 0xEE, 0, 3/s just below 336 -> 320 -> 0x7A
+    assert out["kv_scale"][0] == np.float32(np.float32(4.0) / np.float32(448.0))
+    assert out["kv_nope"][0].tolist() == [0x7E, 0xEE, 0x00, 0x7A]
+    assert out["kv_rope"][0].tolist() == [0x4120, 0x3F80]               # bf16 10, 1: not scaled
+    # block 1: mean nope [1, 1, 1, 1] -> all 448; rotary pair (1, 0) at position 2
+    assert out["kv_scale"][1] == np.float32(np.float32(1.0) / np.float32(448.0))
+    assert out["kv_nope"][1].tolist() == [0x7E] * 4
+    exp = O.encode_bf16(np.array([math.cos(2.0), math.sin(2.0)]))
+    assert out["kv_rope"][1].tolist() == exp.tolist()
+
+
+def test_compress_index_keys_own_bias_no_turn_own_scale():
+    """Indexer keys pool with the bias they are given (here slot 1 dominates, so a key is
+    its block's second token), are not rotated even at a nonzero position, and carry
+    their own e4m3 scale."""
+    ix = np.array([[9, 9, 9, 9],
+                   [-2, 1, 0.5, 0],
+                   [9, 9, 9, 9],
+                   [3, -6, 1.5, 0]], dtype=np.float64)
+    ig = np.zeros_like(ix)
+    out = O.compress_index_keys(ix, ig, np.array([0.0, 50.0]), 2, "e4m3", 0, 2)
+    s0 = np.float32(np.float32(2.0) / np.float32(448.0))
+    s1 = np.float32(np.float32(6.0) / np.float32(448.0))
+    assert out["idx_scale"].tolist() == [s0, s1]
+    assert out["idx_key"][0].tolist() == [0xFE, 0x76, 0x6E, 0x00]       # -448, 224, 112, 0 (units of 2/448)
+    assert out["idx_key"][1].tolist() == [0x76, 0xFE, 0x6E, 0x00]       # 224, -448, 112, 0
+    f = O.compress_index_keys(ix, ig, np.array([0.0, 50.0]), 2, "f32", 1, 1)
+    assert np.allclose(f["idx_key"][0], ix[3], rtol=0, atol=1e-12)
+
+
+def test_query_step_brute_force_tiny():
+    """One CSA query written out with loops: indexer scores over the visible entries,
+    top-k with ties to the lower index, one softmax over the selected entries, the
+    window (rotated at its positions) and the sink."""
+    m, d, dr, n_win, k, theta = 2, 4, 2, 3, 2, 10000.0
+    t = 9                                           # entries 0..4 visible, window 7, 8, 9
+    n_e = 6
+    ent = rng.standard_normal((n_e, d))
+    keys = rng.standard_normal((n_e, 3))
+    q = rng.standard_normal((2, d))
+    qi = rng.standard_normal((2, 3))
+    wi = np.array([0.7, 0.2])
+    sink = np.array([0.3, -1.0])
+    raw = {p: rng.standard_normal(d) for p in range(t + 1)}
+    res = O.query_step("csa", q, t, sink, ent, lambda pos: np.array([raw[int(p)] for p in pos]), m, n_win, dr,
+                       theta, qi, wi, keys, k=k)
+    sc = [sum(wi[h] * max(0.0, sum(qi[h, c] * keys[j, c] for c in range(3))) for h in range(2)) for j in range(5)]
+    order = sorted(range(5), key=lambda j: (-sc[j], j))[:k]
+
+    def turn(v, p):
+        a = p * theta ** 0.0
+        return np.array([v[0], v[1], v[2] * math.cos(a) - v[3] * math.sin(a), v[2] * math.sin(a) + v[3] * math.cos(a)])
+
+    kv = [ent[j] for j in sorted(order)] + [turn(raw[p], p) for p in (7, 8, 9)]
+    for h in range(2):
+        qh = turn(q[h], t)
+        logits = [sum(qh[c] * v[c] for c in range(d)) / math.sqrt(d) for v in kv]
+        den = sum(math.exp(x) for x in logits) + math.exp(sink[h])
+        o = sum(math.exp(x) / den * v for x, v in zip(logits, kv))
+        assert np.allclose(res["o"][h], o, rtol=0, atol=1e-12)
+        assert abs(res["lse"][h] - math.log(den)) < 1e-12
+    assert res["idx"].tolist() == sorted(order) and res["count"] == k
+    assert np.allclose(res["scores"], sc, rtol=0, atol=1e-12)
