@@ -221,7 +221,12 @@ CSA_API csa_status hca_attend(const csa_cache *cache, int batch, int n_q, const 
  *   - The array exists once per device for the life of the process, on every
  *     device that loads the library.  The first call on a device looks up the
  *     array's device address (cudaGetSymbolAddress, with that device current);
- *     make that first call before any stream capture.
+ *     make that first call before any stream capture.  The address is kept for
+ *     the life of the process: after cudaDeviceReset on a device the module is
+ *     loaded afresh and the array may move, so this entry point must not be
+ *     used on that device again in the same process.
+ *   - Device-side failures (a bounded wait of the indexer that gave up) are
+ *     reported by csa_static_status; the rows of such a call get out_count = -1.
  *   - All calls share the one array and its contents outlive a call: calls that
  *     may overlap on the GPU (different streams, or devices sharing a context)
  *     race on it.  Serialise them.  The status word is cleared on each call.
@@ -236,8 +241,30 @@ CSA_API csa_status csa_index_topk_static(const csa_cache *cache, int batch, int 
  * Reads (synchronously, on `stream`) and clears the device status word at the
  * start of a workspace: 0 = fine, otherwise a CSA_ERR_* code set by a kernel
  * whose bounded wait gave up.  Returns CSA_OK or CSA_ERR_CUDA.
+ * The word is sticky: while it is nonzero, every top-k that runs on the workspace
+ * (csa_index_topk, csa_topk given the workspace) writes out_count = -1 and -1
+ * indices for each row instead of selecting from scores that may be incomplete.
  */
 CSA_API csa_status csa_device_status(void *ws, int *status, csa_stream_t stream);
+
+/*
+ * The same for the status word of csa_index_topk_static's scratch on the current
+ * device (that call clears the word when it starts, so this reports its last run).
+ */
+CSA_API csa_status csa_static_status(int *status, csa_stream_t stream);
+
+/*
+ * Failure injection for tests of the bounded waits (process-wide; not for production
+ * use).  The tensor-core indexer's mbarrier waits give up after a number of polls,
+ * record CSA_ERR_TIMEOUT in the status word, drain the copies and MMAs already issued,
+ * free their tensor memory and return; the context stays usable.
+ *   CSA_DEBUG_WAIT_LIMIT:     polls before a wait gives up (0 restores the default, 2^24)
+ *   CSA_DEBUG_STARVE_INDEXER: nonzero makes the indexer's producer issue no key copies,
+ *                             so the first wait for a key tile runs out (0 restores)
+ * Returns CSA_OK or CSA_ERR_INVALID_ARG.
+ */
+enum { CSA_DEBUG_WAIT_LIMIT = 1, CSA_DEBUG_STARVE_INDEXER = 2 };
+CSA_API csa_status csa_debug_set(int knob, long long value);
 
 #ifdef __cplusplus
 }

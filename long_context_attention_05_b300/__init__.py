@@ -21,9 +21,12 @@ LIB_PATH = os.path.join(_HERE, "libcsa.so")
 CSA_F32, CSA_BF16, CSA_E4M3 = 0, 1, 2
 CSA_OK = 0
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "WORKSPACE", 4: "CUDA", 5: "TIMEOUT"}
+STATUS_CODES = {v: k for k, v in STATUS_NAMES.items()}
 
 EXPORTS = ("csa_version", "csa_last_error", "csa_workspace_size", "csa_compress", "csa_index_scores", "csa_topk",
-           "csa_index_topk", "csa_sparse_attend", "hca_attend", "csa_device_status", "csa_index_topk_static")
+           "csa_index_topk", "csa_sparse_attend", "hca_attend", "csa_device_status", "csa_index_topk_static",
+           "csa_static_status", "csa_debug_set")
+CSA_DEBUG_WAIT_LIMIT, CSA_DEBUG_STARVE_INDEXER = 1, 2
 STATIC_SCRATCH_BYTES = 8 << 20
 
 
@@ -64,6 +67,8 @@ def lib() -> ctypes.CDLL:
         L.csa_sparse_attend.argtypes = [C, I, I, P, I, I, P, P, I, P, I, P, P, SZ, P]
         L.hca_attend.argtypes = [C, I, I, P, I, I, P, P, I, P, P, SZ, P]
         L.csa_device_status.argtypes = [P, ctypes.POINTER(I), P]
+        L.csa_static_status.argtypes = [ctypes.POINTER(I), P]
+        L.csa_debug_set.argtypes = [I, ctypes.c_longlong]
         for name in EXPORTS:
             if name not in ("csa_version", "csa_last_error", "csa_workspace_size"):
                 getattr(L, name).restype = I
@@ -252,6 +257,19 @@ def hca_attend(cache: Cache, q, sink, out, out_lse=None, ws=None, stream=None):
 
 
 def device_status(ws: torch.Tensor, stream=None) -> int:
+    """Reads and clears the workspace's device status word (0 = fine, 5 = a bounded wait gave up)."""
     v = ctypes.c_int(0)
     _check(lib().csa_device_status(_ptr(ws), ctypes.byref(v), _stream(stream)), "csa_device_status")
     return v.value
+
+
+def static_status(stream=None) -> int:
+    """Reads and clears the status word of csa_index_topk_static's scratch (current device)."""
+    v = ctypes.c_int(0)
+    _check(lib().csa_static_status(ctypes.byref(v), _stream(stream)), "csa_static_status")
+    return v.value
+
+
+def debug_set(knob: int, value: int) -> None:
+    """Failure injection for tests of the indexer's bounded waits (see include/csa.h)."""
+    _check(lib().csa_debug_set(knob, int(value)), "csa_debug_set")

@@ -6,6 +6,7 @@
 #include <cstdio>
 #include <algorithm>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <string>
 
@@ -14,6 +15,11 @@
 namespace {
 
 thread_local std::string g_err;
+
+// Failure-injection settings of the indexer's bounded waits (csa_debug_set); read at
+// every launch.
+std::atomic<long long> g_wait_limit{0};
+std::atomic<int> g_starve{0};
 
 csa_status fail(csa_status s, const char *fmt, ...) {
   char buf[512];
@@ -220,8 +226,9 @@ cudaError_t launch_indexer(const csa_cache *c, int batch, int n_q, const void *q
   if (hist_used) *hist_used = false;
   if (csa::index_tc_supported(v, heads_idx)) {
     if (hist_used) *hist_used = hist != nullptr;
+    const csa::IndexDebug dbg{g_wait_limit.load(), g_starve.load()};
     return csa::launch_index_tc(v, batch, n_q, q_idx, q_dtype, w, heads_idx, scores, stride, num_sms(),
-                                ws ? (int *)ws : nullptr, hist, st);
+                                ws ? (int *)ws : nullptr, hist, dbg, st);
   }
   return csa::launch_index_generic(v, batch, n_q, q_idx, q_dtype, w, heads_idx, scores, stride, entry_cap(c), st);
 }
@@ -309,15 +316,17 @@ csa_status csa_index_scores(const csa_cache *c, int batch, int n_q, const void *
 
 csa_status csa_topk(const csa_cache *c, int batch, int n_q, const float *scores, int64_t stride, int k,
                     int32_t *out_idx, int32_t *out_count, void *ws, size_t ws_bytes, csa_stream_t stream) {
-  (void)ws; (void)ws_bytes;
   csa_status s = check_cache(c);
   if (s) return s;
   if (batch < 1 || n_q < 1) return fail(CSA_ERR_INVALID_ARG, "batch and n_q must be >= 1");
   if (k < 1) return fail(CSA_ERR_INVALID_ARG, "k must be >= 1");
   if (!scores || !out_idx || !out_count) return fail(CSA_ERR_INVALID_ARG, "NULL pointer");
   if (stride < 1) return fail(CSA_ERR_INVALID_ARG, "scores_stride must be >= 1");
+  if (ws && ((uintptr_t)ws & 255u)) return fail(CSA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  // the workspace's status word (a failed indexer call on it): rows report count -1
+  const int *status = ws && ws_bytes >= kHeader ? (const int *)ws : nullptr;
   return cuda_status(csa::launch_topk(view(c), batch, n_q, scores, stride, k, out_idx, out_count, nullptr, num_sms(),
-                                      (cudaStream_t)stream),
+                                      status, (cudaStream_t)stream),
                      "top-k launch");
 }
 
@@ -341,7 +350,7 @@ csa_status csa_index_topk(const csa_cache *c, int batch, int n_q, const void *q_
                                  hist, &used);
   if (e != cudaSuccess) return cuda_status(e, "indexer launch");
   return cuda_status(csa::launch_topk(view(c), batch, n_q, scores, cap, k, out_idx, out_count, used ? hist : nullptr,
-                                      num_sms(), (cudaStream_t)stream),
+                                      num_sms(), (const int *)ws, (cudaStream_t)stream),
                      "top-k launch");
 }
 
@@ -366,7 +375,7 @@ csa_status csa_index_topk_static(const csa_cache *c, int batch, int n_q, const v
   e = launch_indexer(c, batch, n_q, q_idx, q_dtype, w, heads_idx, scores, cap, ws, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_status(e, "indexer launch");
   return cuda_status(csa::launch_topk(view(c), batch, n_q, scores, cap, k, out_idx, out_count, nullptr, num_sms(),
-                                      (cudaStream_t)stream),
+                                      (const int *)ws, (cudaStream_t)stream),
                      "top-k launch");
 }
 
@@ -383,6 +392,28 @@ csa_status hca_attend(const csa_cache *c, int batch, int n_q, const void *q, int
                       csa_stream_t stream) {
   return attend_common(c, batch, n_q, q, q_dtype, heads, sink, nullptr, 0, out, out_dtype, out_lse, ws, ws_bytes,
                        (cudaStream_t)stream);
+}
+
+csa_status csa_static_status(int *status, csa_stream_t stream) {
+  if (!status) return fail(CSA_ERR_INVALID_ARG, "NULL pointer");
+  csa_status s = CSA_OK;
+  void *ws = static_scratch(s);
+  if (!ws) return s;
+  return csa_device_status(ws, status, stream);
+}
+
+csa_status csa_debug_set(int knob, long long value) {
+  switch (knob) {
+    case CSA_DEBUG_WAIT_LIMIT:
+      if (value < 0) return fail(CSA_ERR_INVALID_ARG, "wait limit must be >= 0");
+      g_wait_limit.store(value);
+      return ok();
+    case CSA_DEBUG_STARVE_INDEXER:
+      g_starve.store(value != 0);
+      return ok();
+    default:
+      return fail(CSA_ERR_INVALID_ARG, "unknown debug knob %d", knob);
+  }
 }
 
 csa_status csa_device_status(void *ws, int *status, csa_stream_t stream) {

@@ -47,7 +47,6 @@ constexpr int kStages = 8;
 constexpr int kStageBytes = kTileM * kDI;
 constexpr int kEpiGroups = 3;   // epilogue warpgroups; group e takes tiles it % 3 == e
 constexpr int kThreads = 64 + 128 * kEpiGroups;
-constexpr long long kWaitLimit = 1LL << 24;
 constexpr int kMaxFlatRows = 256;   // the flat grid serves fewer query rows than this
 
 struct TcArgs {
@@ -62,6 +61,8 @@ struct TcArgs {
   int grid_sms;       // G of the proportional split
   int box_rows;       // rows per TMA box: 128 (contiguous) or the page size
   int *status;        // workspace status word (may be null)
+  long long wait_limit;   // polls before a bounded wait gives up
+  int starve;         // failure injection for tests: the producer issues no key copies
   int q_vec;          // q_idx is 16-byte aligned: vector loads of the query
   unsigned *hist;     // per-row histograms of score-key prefixes (kPrefixBins each), or null
 };
@@ -87,10 +88,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait for the phase of `parity` to complete.  Gives up (returning
-// false) when another role has aborted or after kWaitLimit polls, in which case
+// false) when another role has aborted or after `limit` polls, in which case
 // it raises the abort flag and records CSA_ERR_TIMEOUT.
-__device__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int *status) {
-  for (long long i = 0; i < kWaitLimit; ++i) {
+__device__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int *status, long long limit) {
+  for (long long i = 0; i < limit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63) == 63 && *abort_flag) return false;
   }
@@ -164,6 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
   uint64_t *tempty = tfull + 4;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 4);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  uint64_t *drain = tempty + 5;   // MMA drain after an abort (the 8 bytes after tmem_slot, abort_flag)
   unsigned *shist = reinterpret_cast<unsigned *>(reinterpret_cast<uint8_t *>(tempty + 4) + 16);   // [kPrefixBins]
 
   const CacheView &c = a.c;
@@ -179,6 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
   if (threadIdx.x == 32) {   // barriers (warp 1) while warp 0 works out the partition
     for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
     for (int s = 0; s < 4; ++s) { mbar_init(&tfull[s], 1); mbar_init(&tempty[s], 4); }
+    mbar_init(drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -281,6 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
   const int n_acc = H <= 64 ? 4 : 2;                        // accumulator buffers (2H columns each)
   const uint32_t ncols = H <= 32 ? 256u : 512u;
   uint32_t tmem = 0;
+  int issued = 0;   // key copies the producer issued (lane 0 of warp 0)
   if (warp != 0) {
     if (warp == 1) {   // TMEM first: it does not depend on the query
       asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
@@ -369,7 +373,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
         //      page ids of the next 32 logical pages in flight (lane l holds page
         //      base + l), so no copy waits on a page-table load
       const uint64_t policy = l2_evict_first_policy();
-      int issued = 0;
       const int *ptab = c.page_size ? c.page_table + (long long)b * c.max_pages : nullptr;
       auto page_chunk = [&](long long base) -> int {   // page id of logical page base + lane
         const long long lp = base + lane;
@@ -377,11 +380,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
       };
       long long pbase = -1;
       int pcur = 0, pnext = 0;
-      for (int it = 0; it < n_it; ++it) {
+      for (int it = 0; it < (a.starve ? 0 : n_it); ++it) {
         const int s = it % kStages;
         const uint32_t ph = (uint32_t)(it / kStages) & 1u;
         bool ok = true;
-        if (lane == 0) ok = mbar_wait(&empty[s], ph ^ 1u, abort_flag, a.status);
+        if (lane == 0) ok = mbar_wait(&empty[s], ph ^ 1u, abort_flag, a.status, a.wait_limit);
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;   // warp-uniform
         if (lane == 0) mbar_expect_tx(&full[s], kStageBytes);
         const long long tile = tile_lo + it;
@@ -410,11 +413,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
         }
         ++issued;
       }
-      if (lane == 0 && *abort_flag) {   // let copies already issued land before shared memory goes away
-        for (int it = issued > kStages ? issued - kStages : 0; it < issued; ++it)
-          for (int i = 0; i < (1 << 20) && !mbar_try_wait(&full[it % kStages], (uint32_t)(it / kStages) & 1u); ++i) {
-          }
-      }
     }
   } else if (warp == 1) {
     if (lane == 0) {   // ---- MMA issuer
@@ -426,8 +424,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
         const uint32_t ph = (uint32_t)(it / kStages) & 1u;
         const int acc = it % n_acc;
         const uint32_t aph = (uint32_t)(it / n_acc) & 1u;
-        if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, a.status)) break;
-        if (!mbar_wait(&full[s], ph, abort_flag, a.status)) break;
+        if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, a.status, a.wait_limit)) break;
+        if (!mbar_wait(&full[s], ph, abort_flag, a.status, a.wait_limit)) break;
         tc_fence_after();
         const uint32_t as = su32(stage + s * kStageBytes);
         const uint32_t d = tmem + (uint32_t)(acc * 2 * H);
@@ -480,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
         if (it >= n_it || !live) break;
         const int acc = it % n_acc;
         const uint32_t aph = (uint32_t)(it / n_acc) & 1u;
-        const bool ok = mbar_wait(&tfull[acc], aph, abort_flag, a.status);
+        const bool ok = mbar_wait(&tfull[acc], aph, abort_flag, a.status, a.wait_limit);
         if (!__all_sync(0xffffffffu, ok)) { live = false; break; }   // warp-uniform: TMEM loads are .sync.aligned
         tc_fence_after();
         const uint32_t taddr = tmem + ((uint32_t)(g * 32) << 16) + (uint32_t)(acc * 2 * H);
@@ -524,6 +522,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
   // twice and release the barrier while epilogue warps still read TMEM).
   __syncwarp();
   __syncthreads();
+  if (*abort_flag) {   // uniform: a wait gave up.  Nothing may be in flight when the CTA leaves:
+    if (warp == 0 && lane == 0) {   // the key copies already issued land in shared memory,
+      for (int it = issued > kStages ? issued - kStages : 0; it < issued; ++it)
+        for (int i = 0; i < (1 << 20) && !mbar_try_wait(&full[it % kStages], (uint32_t)(it / kStages) & 1u); ++i) {
+        }
+    }
+    if (warp == 1 && lane == 0) {   // and the MMAs already issued finish before TMEM is freed
+      umma_commit(drain);
+      for (int i = 0; i < (1 << 20) && !mbar_try_wait(drain, 0u); ++i) {
+      }
+    }
+    __syncthreads();
+  }
   if (a.hist) {   // this CTA's prefix counts into the row's histogram
     for (int e = threadIdx.x; e < kPrefixBins; e += kThreads) {
       const unsigned v = shist[e];
@@ -568,7 +579,7 @@ size_t index_tc_smem_bytes() {
 
 cudaError_t launch_index_tc(const CacheView &c, int batch, int n_q, const void *q_idx, int q_dtype, const float *w,
                             int heads_idx, float *scores, long long stride, int num_sms, int *status,
-                            unsigned *hist, cudaStream_t st) {
+                            unsigned *hist, const IndexDebug &dbg, cudaStream_t st) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   CUtensorMap map;
@@ -588,6 +599,8 @@ cudaError_t launch_index_tc(const CacheView &c, int batch, int n_q, const void *
   a.c = c; a.n_q = n_q; a.heads = heads_idx; a.q_dtype = q_dtype;
   a.q_idx = (const uint8_t *)q_idx; a.w = w; a.scores = scores; a.stride = stride;
   a.box_rows = box_rows; a.status = status;
+  a.wait_limit = dbg.wait_limit > 0 ? dbg.wait_limit : (1LL << 24);
+  a.starve = dbg.starve;
   a.q_vec = ((uintptr_t)q_idx & 15) == 0;
   a.hist = hist;
   const int rows_q = batch * n_q;

@@ -42,11 +42,19 @@ cudaError_t launch_index_generic(const CacheView &c, int batch, int n_q, const v
                                  const float *w, int heads_idx, float *scores, long long stride,
                                  long long n_cap, cudaStream_t st);
 
+// Test hooks of the tensor-core indexer's bounded waits (failure injection):
+// wait_limit = polls before a wait gives up (0: the default, 2^24); starve = 1 makes
+// the producer issue no key copies, so the MMA warp's first wait runs out.
+struct IndexDebug {
+  long long wait_limit;
+  int starve;
+};
+
 bool index_tc_supported(const CacheView &c, int heads_idx);
 size_t index_tc_smem_bytes();
 cudaError_t launch_index_tc(const CacheView &c, int batch, int n_q, const void *q_idx, int q_dtype, const float *w,
                             int heads_idx, float *scores, long long stride, int num_sms, int *status,
-                            unsigned *hist, cudaStream_t st);
+                            unsigned *hist, const IndexDebug &dbg, cudaStream_t st);
 
 // Histogram of the top kPrefixBits bits of the order-preserving score keys, one per
 // query row: the tensor-core indexer fills it (when given one) while it scores, and
@@ -56,7 +64,8 @@ constexpr int kPrefixBins = 1 << kPrefixBits;
 constexpr int kPrefixRowsMax = 256;   // rows served with prefix histograms (decode-sized calls)
 
 cudaError_t launch_topk(const CacheView &c, int batch, int n_q, const float *scores, long long stride, int k,
-                        int32_t *out_idx, int32_t *out_count, unsigned *hist, int num_sms, cudaStream_t st);
+                        int32_t *out_idx, int32_t *out_count, unsigned *hist, int num_sms, const int *status,
+                        cudaStream_t st);
 
 constexpr int kHG = 16;
 constexpr int kKC = 32;

@@ -43,9 +43,15 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *buf, int &total)
   return (w ? buf[32 + w - 1] : 0) + x - v;
 }
 
+// A nonzero status word (the indexer's bounded wait gave up, so the scores are
+// incomplete): the row gets count -1 and all-(-1) indices instead of a selection.
+__device__ __forceinline__ bool status_failed(const int *status) {
+  return status != nullptr && *reinterpret_cast<const volatile int *>(status) != 0;
+}
+
 __global__ void __launch_bounds__(kTopkThreads) k_topk_row(CacheView c, int n_q, const float *scores,
                                                            long long stride, int k, int32_t *out_idx,
-                                                           int32_t *out_count) {
+                                                           int32_t *out_count, const int *status) {
   __shared__ unsigned hist[256];
   __shared__ int scan_buf[64];
   __shared__ unsigned sh_prefix;
@@ -59,9 +65,10 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_row(CacheView c, int n_q,
   if (n > stride) n = stride;
   const float *s = scores + (long long)row * stride;
   int32_t *out = out_idx + (long long)row * k;
-  if (n <= k) {
-    for (int j = threadIdx.x; j < k; j += blockDim.x) out[j] = j < n ? j : -1;
-    if (threadIdx.x == 0) out_count[row] = (int32_t)n;
+  const bool failed = status_failed(status);
+  if (n <= k || failed) {
+    for (int j = threadIdx.x; j < k; j += blockDim.x) out[j] = (j < n && !failed) ? j : -1;
+    if (threadIdx.x == 0) out_count[row] = failed ? -1 : (int32_t)n;
     return;
   }
   unsigned prefix = 0, mask = 0;
@@ -150,7 +157,8 @@ __device__ __forceinline__ float key_float(unsigned key) {
 
 __global__ void __launch_bounds__(kTopkThreads) k_topk_cluster(CacheView c, int n_q, const float *scores,
                                                                long long stride, int k, int32_t *out_idx,
-                                                               int32_t *out_count, unsigned *ghist, int slice_cap) {
+                                                               int32_t *out_count, unsigned *ghist, int slice_cap,
+                                                               const int *status) {
   namespace cg = cooperative_groups;
   cg::cluster_group cl = cg::this_cluster();
   extern __shared__ unsigned keys[];             // [slice_cap] keys, then [slice_cap] uint16 bins
@@ -179,10 +187,11 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_cluster(CacheView c, int 
   long long n = min((t + 1) / c.m, c.cap);
   if (n > stride) n = stride;
   int32_t *out = out_idx + (long long)row * k;
-  if (n <= k) {   // uniform over the cluster: no cluster barrier is reached
+  const bool failed = status_failed(status);   // the same word for every CTA of the cluster
+  if (n <= k || failed) {   // uniform over the cluster: no cluster barrier is reached
     if (rank == 0) {
-      for (int j = threadIdx.x; j < k; j += blockDim.x) out[j] = j < n ? j : -1;
-      if (threadIdx.x == 0) out_count[row] = (int32_t)n;
+      for (int j = threadIdx.x; j < k; j += blockDim.x) out[j] = (j < n && !failed) ? j : -1;
+      if (threadIdx.x == 0) out_count[row] = failed ? -1 : (int32_t)n;
     }
     return;
   }
@@ -671,7 +680,8 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_cluster(CacheView c, int 
 // Rows with few queries get a cluster of up to 16 CTAs each; many rows get one
 // CTA each.  Rows whose slice would not fit in shared memory use k_topk_row.
 cudaError_t launch_topk(const CacheView &c, int batch, int n_q, const float *scores, long long stride, int k,
-                        int32_t *out_idx, int32_t *out_count, unsigned *hist, int num_sms, cudaStream_t st) {
+                        int32_t *out_idx, int32_t *out_count, unsigned *hist, int num_sms, const int *status,
+                        cudaStream_t st) {
   const int rows = batch * n_q;
   const long long n_cap = c.cap < stride ? c.cap : stride;
   // the row kernel does not read the indexer's prefix histograms; they are left zeroed
@@ -682,7 +692,7 @@ cudaError_t launch_topk(const CacheView &c, int batch, int n_q, const float *sco
       if (e != cudaSuccess) return e;
     }
     return launch_pdl(k_topk_row, dim3(rows), dim3(kTopkThreads), 0, st, 1, c, n_q, scores, stride, k, out_idx,
-                      out_count);
+                      out_count, status);
   };
   // cluster size: up to 16 CTAs per row for few rows; with many rows, halve it while
   // the grid exceeds two waves and the halved slices still fit in shared memory
@@ -703,7 +713,7 @@ cudaError_t launch_topk(const CacheView &c, int batch, int n_q, const float *sco
     const size_t sm = (size_t)((n_cap + cs - 1) / cs) * 6;
     if (sm > 160 * 1024) break;
     e = launch_pdl(k_topk_cluster, dim3(cs, rows), dim3(kTopkThreads), sm, st, cs, c, n_q, scores, stride, k, out_idx,
-                   out_count, hist, (int)((n_cap + cs - 1) / cs));
+                   out_count, hist, (int)((n_cap + cs - 1) / cs), status);
     if (e == cudaSuccess || cs == 1) return e;
     cudaGetLastError();   // cluster too large for this device: halve it
   }

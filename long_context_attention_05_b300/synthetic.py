@@ -122,6 +122,12 @@ class Workload:
             return 0
         return -(-self.max_entries // self.page_size)
 
+    def pages_needed(self, b):
+        """Pages sequence b owns in a paged cache: its entries, the step's new ones and
+        the spare capacity (the longest sequence needs max_pages)."""
+        cap = self.n_entries[b] + self.n_new // self.m + 1 + self.extra_entries
+        return -(-cap // self.page_size)
+
 
 def config0(**kw) -> Workload:
     """Single CSA layer decode in FP32: batch 1, 4096 context tokens, m=4 (1024
@@ -263,11 +269,8 @@ def seeded_cache(w: Workload, q_idx: Optional[np.ndarray] = None, w_idx: Optiona
     B, d, dr = w.batch, w.d, w.d_rope
     dn = d - dr
     if w.page_size:
-        pages_per_seq = w.max_pages
-        n_pages = B * pages_per_seq + w.spare_pages
+        n_pages, page_table = page_layout(w)
         rows = n_pages * w.page_size
-        perm = _rng(w.seed, _S_PAGES).permutation(n_pages).astype(np.int32)
-        page_table = perm[: B * pages_per_seq].reshape(B, pages_per_seq).copy()
     else:
         rows = B * w.max_entries
         page_table = None
@@ -313,7 +316,7 @@ def seeded_cache(w: Workload, q_idx: Optional[np.ndarray] = None, w_idx: Optiona
 def empty_cache(w: Workload) -> Dict[str, np.ndarray]:
     """Zeroed cache storage (the compressor fills it)."""
     B, d, dr = w.batch, w.d, w.d_rope
-    rows = B * w.max_entries if not w.page_size else (B * w.max_pages + w.spare_pages) * w.page_size
+    rows = B * w.max_entries if not w.page_size else page_layout(w)[0] * w.page_size
     out: Dict[str, np.ndarray] = {}
     if w.kv_dtype == "e4m3":
         out["kv_nope"] = np.zeros((rows, d - dr), np.uint8)
@@ -331,10 +334,25 @@ def empty_cache(w: Workload) -> Dict[str, np.ndarray]:
     out["pool_state"] = np.zeros((B, 3 * (d + w.d_idx)), dtype=np.float32)
     out["n_tokens"] = np.zeros((B,), dtype=np.int64)
     if w.page_size:
-        n_pages = B * w.max_pages + w.spare_pages
-        perm = _rng(w.seed, _S_PAGES).permutation(n_pages).astype(np.int32)
-        out["page_table"] = perm[: B * w.max_pages].reshape(B, w.max_pages).copy()
+        out["page_table"] = page_layout(w)[1]
     return out
+
+
+def page_layout(w: Workload):
+    """Physical pages of a paged cache: sequence b owns pages_needed(b) pages, taken
+    from a seeded permutation of the pool (plus spare_pages unused ones).  The page
+    table is [batch, max_pages]; slots past a sequence's own pages repeat its last
+    page (they are never read for data)."""
+    need = [w.pages_needed(b) for b in range(w.batch)]
+    n_pages = sum(need) + w.spare_pages
+    perm = _rng(w.seed, _S_PAGES).permutation(n_pages).astype(np.int32)
+    table = np.empty((w.batch, w.max_pages), dtype=np.int32)
+    off = 0
+    for b, nb in enumerate(need):
+        table[b, :nb] = perm[off:off + nb]
+        table[b, nb:] = perm[off + nb - 1]
+        off += nb
+    return n_pages, table
 
 
 def _rows_of(w: Workload, page_table, b, js):
