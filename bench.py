@@ -171,6 +171,12 @@ def job_throughput(world, queries_per_rank_step, steps, seconds):
     return world * queries_per_rank_step * steps / seconds
 
 
+def _total_steps(args):
+    """Steps the GPU arm runs on one cache (warm-up, timed, graph warm-up, end to end):
+    sizes the spare entry capacity, which both arms use so they see the same bytes."""
+    return args.steps * 3 + args.warmup + 8
+
+
 def _workload(name, steps_total):
     from long_context_attention_05_b300 import synthetic as S
     extra = steps_total // 4 + 16
@@ -205,14 +211,16 @@ def _alg_bytes(w):
     return idx_bytes, idx_bytes + att + q_bytes + out_bytes + new_tok + win
 
 
-def _oracle_rows_inproc(workload, budget_s, n_layers, steps=1, warmup=0):
+def _oracle_rows_inproc(workload, budget_s, n_layers, steps=1, warmup=0, dump=None, steps_total=0):
     """Times the oracle on whole query rows (one sequence's query at a time):
     `warmup` untimed rows, then `steps` sample steps of at least one row each,
-    together about budget_s seconds.  Inputs are generated once."""
+    together about budget_s seconds.  Inputs are generated once.  With `dump`, the
+    oracle's result of every row it computed (first time) is saved there (npz) for
+    the parity summary of the benchmark line."""
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     import harness as H
     from long_context_attention_05_b300 import synthetic as S
-    wl = _workload(workload, 0)[:n_layers]
+    wl = _workload(workload, steps_total)[:n_layers]   # the GPU arm's sizes: the same seeded bytes
     data = []
     for w in wl:
         inp = S.step_inputs(w)
@@ -221,6 +229,7 @@ def _oracle_rows_inproc(workload, budget_s, n_layers, steps=1, warmup=0):
         data.append((w, inp, arrs, rows))
     order = [(li, r) for r in range(max(len(d[3]) for d in data)) for li in range(len(data)) if r < len(data[li][3])]
     pos = 0
+    kept = {}
 
     def one_row():
         nonlocal pos
@@ -229,8 +238,11 @@ def _oracle_rows_inproc(workload, budget_s, n_layers, steps=1, warmup=0):
         w, inp, arrs, rows = data[li]
         b, i = rows[r]
         t0 = time.perf_counter()
-        H.oracle_seeded_step(w, arrs, inp, b, i)
-        return time.perf_counter() - t0
+        ref = H.oracle_seeded_step(w, arrs, inp, b, i)
+        dt = time.perf_counter() - t0
+        if dump is not None and (li, b, i) not in kept:
+            kept[(li, b, i)] = ref
+        return dt
 
     for _ in range(warmup):
         one_row()
@@ -244,27 +256,89 @@ def _oracle_rows_inproc(workload, budget_s, n_layers, steps=1, warmup=0):
             if t_step >= per_step:
                 break
         t_total += t_step
+    if dump is not None:
+        out = {}
+        for n, ((li, b, i), ref) in enumerate(kept.items()):
+            out[f"r{n}_key"] = np.array([li, b, i])
+            for f in ("o", "lse", "idx", "scores", "slack"):
+                if f in ref:
+                    out[f"r{n}_{f}"] = np.asarray(ref[f])
+            if "count" in ref:
+                out[f"r{n}_count"] = np.array(ref["count"])
+        np.savez(dump, **out)
     return n_rows, t_total
 
 
-def _oracle_rows(workload, budget_s, n_layers=1, steps=1, warmup=0):
+def _oracle_rows(workload, budget_s, n_layers=1, steps=1, warmup=0, dump=None, steps_total=0):
     """Runs the oracle sample in a fresh single-threaded process (BLAS and OpenMP
     pinned to one thread; spawned, never forked from a CUDA process)."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                NUMEXPR_NUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-sample", workload, str(budget_s),
-                        str(n_layers), str(steps), str(warmup)], capture_output=True, text=True, env=env)
+                        str(n_layers), str(steps), str(warmup), dump or "", str(steps_total)],
+                       capture_output=True, text=True, env=env)
     if r.returncode != 0:
         raise RuntimeError("oracle sample failed:\n" + r.stderr[-2000:])
     d = json.loads(r.stdout.strip().splitlines()[-1])
     return d["rows"], d["seconds"]
 
 
+def parity_summary(dump, gpu_rows):
+    """GPU results of the benchmark's first step against the oracle rows of the CPU
+    baseline (same seeded inputs): per row, the top-k set (differences allowed only
+    for near-ties within 1e-6 relative of the oracle's k-th score) and the largest
+    |gpu - oracle| of the output relative to the row's largest |oracle| value
+    (tolerance 2e-3 plus half a bf16 ulp of the oracle value, the output's own
+    rounding)."""
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import harness as H
+    z = np.load(dump)
+    n_rows = len([k for k in z.files if k.endswith("_key")])
+    ties = bad_sets = bad_out = 0
+    worst, worst_lse = 0.0, 0.0
+    for n in range(n_rows):
+        li, b, i = (int(x) for x in z[f"r{n}_key"])
+        g = gpu_rows.get((li, b, i))
+        if g is None:
+            continue
+        o_ref, lse_ref = z[f"r{n}_o"], z[f"r{n}_lse"]
+        tie_row = False
+        if f"r{n}_idx" in z.files:
+            try:
+                nt = H.check_topk(g["idx"], g["cnt"], z[f"r{n}_idx"], int(z[f"r{n}_count"]), z[f"r{n}_scores"],
+                                  "bench", slack=z[f"r{n}_slack"])
+                ties += nt
+                tie_row = nt > 0
+            except AssertionError:
+                bad_sets += 1
+                continue
+        if tie_row:   # outputs differ legitimately when a near-tie flipped the set
+            continue
+        worst = max(worst, float(H.row_rel_err(g["o"], o_ref).max()))
+        worst_lse = max(worst_lse, float(np.abs(g["lse"] - lse_ref).max()))
+        allow = H.TOL_LOW * np.abs(o_ref).max(axis=-1, keepdims=True) + H.bf16_half_ulp(o_ref)
+        bad_out += int((np.abs(g["o"] - o_ref) > allow).any())
+    return {"rows": n_rows, "near_tie_flips": ties, "topk_mismatch_rows": bad_sets, "out_fail_rows": bad_out,
+            "max_row_rel_err_out": worst, "max_abs_err_lse": worst_lse,
+            "tolerance": "2e-3 of the row max + half a bf16 ulp (bf16 output)", "pass": bad_sets == 0 and bad_out == 0}
+
+
+def config_dict(wl, workload):
+    """The benchmark line's config: the workload and its sizes (shared by both arms)."""
+    w0l = wl[0]
+    return {"workload": w0l.name if len(wl) == 1 else workload, "batch_per_gpu": w0l.batch,
+            "ctx_tokens": int(max(w0l.ctx)), "entries_per_seq": int(max(w0l.n_entries)), "m": w0l.m,
+            "heads": w0l.heads, "d": w0l.d, "indexer": f"{w0l.heads_idx}x{w0l.d_idx} e4m3", "top_k": w0l.k,
+            "window": w0l.n_win, "layers": len(wl), "new_tokens_per_seq": w0l.n_new,
+            "l2": "inputs larger than L2 (cache >> 126 MB)"}
+
+
 def run_reference(args):
-    wl = _workload(args.workload, 0)
+    wl = _workload(args.workload, _total_steps(args))
     n_layers = 2 if args.workload == "stack_decode_paged" else 1
     per_step = args.budget / max(args.steps, 1)
-    rows_total, t_total = _oracle_rows(args.workload, args.budget, n_layers, args.steps, args.warmup)
+    rows_total, t_total = _oracle_rows(args.workload, args.budget, n_layers, args.steps, args.warmup,
+                                       steps_total=_total_steps(args))
     qps = rows_total / t_total
     if n_layers == 2:   # a query of the stack is one row in each of its 4 layers (2 CSA, 2 HCA)
         qps /= 2.0
@@ -275,7 +349,7 @@ def run_reference(args):
             "warmup": args.warmup, "ms_per_step": 1000.0 * t_total / max(args.steps, 1),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded caches, no weights)",
-            "config": {"workload": wl[0].name if n_layers == 1 else args.workload},
+            "config": config_dict(wl, args.workload),
             "cpu_baseline": {"value": qps, "unit": "queries/s", "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": qps, "unit": "queries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -309,7 +383,7 @@ def run_ours(args, rank, world, local_rank):
     from long_context_attention_05_b300 import synthetic as S
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    total_steps = args.steps * 3 + args.warmup + 8
+    total_steps = _total_steps(args)
     wl = _workload(args.workload, total_steps)
     nsets = 4
     layers = []
@@ -354,6 +428,23 @@ def run_ours(args, rank, world, local_rank):
             else:
                 L.hca_attend(c, gi["q"], gi["sink"], b["out"], b["lse"], ly["ws"])
 
+    # the first step on the freshly seeded caches is the one the oracle rows of the CPU
+    # baseline describe: keep its results for the parity summary
+    gpu_rows = {}
+    if not args.no_cpu_baseline and world == 1 and rank == 0:
+        launches(0, None)
+        torch.cuda.synchronize(dev)
+        for li, ly in enumerate(layers[:2]):
+            w, b = ly["w"], ly["bufs"]
+            o = b["out"].float().cpu().numpy().astype(np.float64)
+            lse = b["lse"].cpu().numpy().astype(np.float64)
+            idx = b["idx"].cpu().numpy() if "idx" in b else None
+            cnt = b["cnt"].cpu().numpy() if "cnt" in b else None
+            for bb in range(w.batch):
+                for i in range(w.n_new):
+                    gpu_rows[(li, bb, i)] = {"o": o[bb, i], "lse": lse[bb, i],
+                                             "idx": None if idx is None else idx[bb, i],
+                                             "cnt": None if cnt is None else int(cnt[bb, i])}
     # eager warm-up; then the timed region is ONE CUDA graph holding all K steps
     # (so host launch overhead cannot set the pace), and the indexer is timed alone
     # as K back-to-back launches in its own graph
@@ -392,14 +483,16 @@ def run_ours(args, rank, world, local_rank):
     barrier()
     torch.cuda.synchronize(dev)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local_rank) as clk:
-        t0.record(stream)
-        if g_steps is not None:
-            g_steps.replay()
-        else:
-            steps_fn(args.warmup, args.steps)()
-        t1.record(stream)
-        torch.cuda.synchronize(dev)
+    # clocks are sampled from just before the timed region to the end of the end-to-end
+    # loop (nvidia-smi polls every 100 ms; the timed region alone is a few ms)
+    clk = ClockSampler(local_rank).__enter__()
+    t0.record(stream)
+    if g_steps is not None:
+        g_steps.replay()
+    else:
+        steps_fn(args.warmup, args.steps)()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
     barrier()
     torch.cuda.synchronize(dev)
     ms = t0.elapsed_time(t1)
@@ -443,6 +536,7 @@ def run_ours(args, rank, world, local_rank):
             e2e_fn(k)()
     torch.cuda.synchronize(dev)
     e2e_s = time.perf_counter() - w0
+    clk.__exit__(None, None, None)
     barrier()
 
     if world > 1:
@@ -468,29 +562,30 @@ def run_ours(args, rank, world, local_rank):
     if rank != 0:
         return
     cpu = None
+    parity = None
     if not args.no_cpu_baseline and world == 1:
+        import tempfile
         nl = 2 if args.workload == "stack_decode_paged" else 1
-        n, t = _oracle_rows(args.workload, args.budget, nl)
+        dump = os.path.join(tempfile.mkdtemp(prefix="csa_bench_"), "oracle_rows.npz")
+        n, t = _oracle_rows(args.workload, args.budget, nl, dump=dump, steps_total=total_steps)
         qps = n / t / float(nl)
         cpu = {"value": qps, "unit": "queries/s", "cores": 1, "kind": "oracle",
                "sample": f"{n} oracle query rows of {w0l.name} (fp64 numpy, 1 thread), {t:.1f} s"}
+        parity = parity_summary(dump, gpu_rows)
     gqa8 = 8 * 128 * 2 * 2
     line = {
         "metric": "CSA/HCA decode queries/s at 1M ctx; achieved HBM GB/s vs B300 peak",
         "value": value, "unit": "queries/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3/bf16 storage, f32 accumulate", "data": "synthetic (seeded caches, no weights)",
-        "config": {"workload": w0l.name if len(layers) == 1 else args.workload, "batch_per_gpu": w0l.batch,
-                   "ctx_tokens": int(max(w0l.ctx)), "entries_per_seq": int(max(w0l.n_entries)), "m": w0l.m,
-                   "heads": w0l.heads, "d": w0l.d, "indexer": f"{w0l.heads_idx}x{w0l.d_idx} e4m3", "top_k": w0l.k,
-                   "window": w0l.n_win, "layers": len(layers),
-                   "l2": "inputs larger than L2 (cache >> 126 MB)",
-                   "kv_bytes_per_token_vs_bf16_gqa8": round(sum(ly["kv_bytes"] for ly in layers) /
-                                                            (len(layers) * w0l.batch * max(w0l.ctx)) / gqa8, 4)},
+        "config": dict(config_dict([ly["w"] for ly in layers], args.workload),
+                       kv_bytes_per_token_vs_bf16_gqa8=round(sum(ly["kv_bytes"] for ly in layers) /
+                                                             (len(layers) * sum(w0l.ctx)) / gqa8, 4)),
         "roofline": roofline,
         "step_roofline": {"bound": "hbm", "achieved": round(step_ach, 1), "peak": hbm_peak, "unit": "GB/s",
                           "frac": round(step_ach / hbm_peak, 4), "alg_bytes_per_step": int(step_bytes_all)},
         "cpu_baseline": cpu,
+        "parity": parity,
         "e2e": {"value": e2e, "unit": "queries/s", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
@@ -501,7 +596,8 @@ def run_ours(args, rank, world, local_rank):
 def main():
     if len(sys.argv) > 1 and sys.argv[1] == "--oracle-sample":
         n, t = _oracle_rows_inproc(sys.argv[2], float(sys.argv[3]), int(sys.argv[4]), int(sys.argv[5]),
-                                   int(sys.argv[6]))
+                                   int(sys.argv[6]), dump=(sys.argv[7] if len(sys.argv) > 7 and sys.argv[7] else None),
+                                   steps_total=int(sys.argv[8]) if len(sys.argv) > 8 else 0)
         print(json.dumps({"rows": n, "seconds": t}))
         return
     ap = argparse.ArgumentParser()
