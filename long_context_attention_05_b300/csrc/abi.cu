@@ -181,6 +181,8 @@ csa_status attend_common(const csa_cache *c, int batch, int n_q, const void *q, 
   if (q_dtype != CSA_BF16 && q_dtype != CSA_F32) return fail(CSA_ERR_INVALID_ARG, "q_dtype must be BF16 or F32");
   if (out_dtype != CSA_BF16 && out_dtype != CSA_F32) return fail(CSA_ERR_INVALID_ARG, "out_dtype must be BF16 or F32");
   if (idx && k < 1) return fail(CSA_ERR_INVALID_ARG, "k must be >= 1");
+  if (((uintptr_t)q & 15) || ((uintptr_t)out & 7) || ((uintptr_t)idx & 3) || ((uintptr_t)out_lse & 3))
+    return fail(CSA_ERR_INVALID_ARG, "q must be 16-byte, out 8-byte, idx and out_lse 4-byte aligned");
   if (csa::attend_smem_bytes(c->d) > 227 * 1024) return fail(CSA_ERR_UNSUPPORTED, "d=%d too large", c->d);
   const long long list_cap = idx ? (long long)k : entry_cap(c);
   const AttendPlan p = attend_plan(c, batch, n_q, heads, list_cap);

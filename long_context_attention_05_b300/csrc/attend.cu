@@ -9,8 +9,9 @@
 // attends to the top-k blocks plus a window of uncompressed recent tokens; HCA
 // attends densely to all 128-token entries with the same window.
 //
-// Key space of one query row: u < n_list are entries (CSA: idx[row][u], HCA:
-// entry u), n_list <= u < n_list + n_win are window tokens t-n_win+1 .. t.  A CTA
+// Key space of one query row: u < n_win are the window tokens t-n_win+1 .. t,
+// n_win <= u < n_win + n_list the entries (CSA: idx[row][u - n_win], HCA: entry
+// u - n_win), the order the tensor-core kernel uses.  A CTA
 // handles HG heads of one row and a contiguous range of KC-key chunks with an
 // online softmax; with one split it also adds the sink and writes the output,
 // otherwise it writes (max, sum, weighted sum) partials that k_attend_combine
@@ -78,12 +79,13 @@ __global__ void __launch_bounds__(kAttThreads) k_attend(AttendArgs a) {
     if (tid < kKC) {
       const long long u = u0 + tid;
       long long src = -1;
-      if (u < n_list) {
-        const long long j = a.idx ? (long long)a.idx[(long long)row * a.k + u] : u;
-        if (j >= 0 && j < n_vis) src = entry_row(c, b, j);
-      } else if (u < U) {
-        const long long tau = t - c.n_win + 1 + (u - n_list);
+      if (u < c.n_win) {
+        const long long tau = t - c.n_win + 1 + u;
         if (tau >= 0) src = -2 - tau;
+      } else if (u < U) {
+        const long long e = u - c.n_win;
+        const long long j = a.idx ? (long long)a.idx[(long long)row * a.k + e] : e;
+        if (j >= 0 && j < n_vis) src = entry_row(c, b, j);
       }
       ksrc[tid] = src;
     }
@@ -285,10 +287,12 @@ __global__ void __launch_bounds__(kCombThreads) k_attend_combine(AttendArgs a) {
 // Split plan shared by the launcher and the workspace sizing.  It depends only
 // on the key-list capacity and on whether the call is a decode (one query per
 // sequence), never on the batch, so a row's reduction order -- and its bits --
-// do not change with the other rows in the batch.  Decode: one 64-key chunk
+// do not change with the other rows in the batch.  Decode: two 64-key chunks
 // per CTA (tensor-core kernel) or four 32-key chunks (CUDA-core kernel), merged
-// by k_attend_combine.  Prefill (many queries per
-// sequence): one CTA walks all chunks of its row.
+// by k_attend_combine.  Prefill (many queries per sequence): one CTA walks all
+// chunks of its row.  The window comes first in a row's key list, so splits past
+// the last key hold only absent keys: a longer list of the same keys adds splits
+// whose partials weigh exactly zero in the merge.
 void attend_plan(int n_q, long long list_cap, int n_win, bool tc, int &n_splits, int &cps) {
   const int keys = tc ? 64 : kKC;               // keys per chunk of the kernel that runs
   const long long chunks = (list_cap + n_win + keys - 1) / keys;
@@ -297,7 +301,7 @@ void attend_plan(int n_q, long long list_cap, int n_win, bool tc, int &n_splits,
     n_splits = 1;
     return;
   }
-  cps = tc ? 1 : 4;
+  cps = tc ? 2 : 4;
   n_splits = (int)((chunks + cps - 1) / cps);
 }
 

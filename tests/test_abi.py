@@ -47,8 +47,8 @@ def test_workspace_size_and_geometry_checks():
     n = lib.csa_workspace_size(ctypes.byref(s), 4, 1, 64, 2048)
     # scores for 4 rows x 1000 entries, and split partials of the decode attention
     assert n >= 256 + 4 * 1000 * 4
-    chunks = -(-(2048 + 128) // 32)
-    splits = -(-chunks // 4)
+    chunks = -(-(2048 + 128) // 64)            # tensor-core attention: 64-key chunks, 2 per split
+    splits = -(-chunks // 2)
     assert n >= 256 + 4 * splits * 64 * 512 * 4
     assert lib.csa_workspace_size(ctypes.byref(_struct(d=500)), 4, 1, 64, 2048) == 0
     assert lib.csa_workspace_size(ctypes.byref(_struct(d_idx=100)), 4, 1, 64, 2048) == 0
@@ -109,7 +109,7 @@ def _expected_workspace(batch, n_q, heads, k, d=512, n_win=128, entry_cap=1000):
     histograms of 8192 score-key prefixes at the end."""
     rows = batch * n_q
     chunks = -(-(k + n_win) // 64)              # tensor-core attention: 64-key chunks
-    splits = chunks if n_q == 1 else 1          # decode: one chunk per split
+    splits = -(-chunks // 2) if n_q == 1 else 1  # decode: two chunks per split
     parts = rows * splits * heads
     part_bytes = (_align256(parts * d * 4) + _align256(parts * 2 * 4)) if splits > 1 else 0
     need = max(256 + _align256(rows * entry_cap * 4), 256 + part_bytes)

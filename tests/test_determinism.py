@@ -82,3 +82,47 @@ def test_paged_equals_contiguous():
     ap["page_table"] = pt
     paged = H.gpu_seeded_step(wp, ap, inp)
     _same(cont, paged)
+
+
+def test_padded_key_list_is_bitwise_identical():
+    """The window comes first in a row's key list, so padding the selected entries with
+    absent (-1) slots adds only chunks and splits of absent keys, whose partials weigh
+    exactly zero: the same bits for k = 512 and the same list padded to 640 and 1024."""
+    import long_context_attention_05_b300 as L
+    w = S.config2(ctx=(65536, 40000, 8192, 100000), k=512)
+    arrs, inp = _setup(w)
+    base = H.gpu_seeded_step(w, arrs, inp, chained=True)
+    cache, gi, ws0 = base["cache"], base["gi"], base["ws"]
+    idx = torch.from_numpy(base["idx"]).cuda()
+    outs = []
+    for k in (512, 640, 1024):
+        pad = torch.full((w.batch, 1, k), -1, dtype=torch.int32, device="cuda")
+        pad[:, :, :512] = idx
+        ws = L.alloc_workspace(cache, w.batch, 1, w.heads, k)
+        out = torch.empty((w.batch, 1, w.heads, w.d), dtype=torch.float32, device="cuda")
+        lse = torch.empty((w.batch, 1, w.heads), dtype=torch.float32, device="cuda")
+        L.csa_sparse_attend(cache, gi["q"], gi["sink"], pad, out, lse, ws)
+        torch.cuda.synchronize()
+        outs.append((out.cpu().numpy(), lse.cpu().numpy()))
+    for k, (o, l) in zip((640, 1024), outs[1:]):
+        assert np.array_equal(o, outs[0][0]) and np.array_equal(l, outs[0][1]), k
+
+
+def test_dense_rows_do_not_depend_on_the_entry_capacity():
+    """HCA's split plan covers the cache's entry capacity; splits past a row's keys do
+    nothing, so the capacity (and the split count it gives) leaves the bits unchanged."""
+    import dataclasses
+    w = S.config1(batch=3, ctx=(131072, 65536, 1024))
+    arrs, inp = _setup(w)
+    a = H.gpu_seeded_step(w, arrs, inp)
+    w2 = dataclasses.replace(w, extra_entries=w.extra_entries + 3000)
+    rows2 = w2.max_entries
+    a2 = dict(arrs)
+    for name in ("kv_nope", "kv_scale", "kv_rope"):
+        src = arrs[name]
+        dst = np.zeros((w.batch * rows2,) + src.shape[1:], dtype=src.dtype)
+        for b in range(w.batch):
+            dst[b * rows2:b * rows2 + w.max_entries] = src[b * w.max_entries:(b + 1) * w.max_entries]
+        a2[name] = dst
+    b2 = H.gpu_seeded_step(w2, a2, inp)
+    _same(a, b2)
