@@ -63,7 +63,16 @@ enum {
   CSA_ERR_TIMEOUT = 5        /* a device-side bounded wait gave up (csa_device_status) */
 };
 
-enum { CSA_F32 = 0, CSA_BF16 = 1, CSA_E4M3 = 2 };
+/*
+ * Element types.  CSA_BF16_Q_E4M3 is accepted only as the q_dtype of the indexer
+ * calls: the query-side FP8 variant of the lightning indexer ([S] "Two kinds of
+ * memory instead of one": the indexer runs in low precision).  The query is
+ * passed as bf16; the indexer quantises each (query, head) vector to e4m3 with a
+ * power-of-two scale S (max|q_h| * S in [2^7, 2^8), round to nearest even) and
+ * scores with q_h' = e4m3(q_h * S) / S.  The default (CSA_BF16) scores with the
+ * bf16 query itself.
+ */
+enum { CSA_F32 = 0, CSA_BF16 = 1, CSA_E4M3 = 2, CSA_BF16_Q_E4M3 = 3 };
 
 /*
  * One layer's compressed cache.  Geometry fields are host values; pointers are
@@ -153,7 +162,8 @@ CSA_API csa_status csa_compress(const csa_cache *cache, int batch, int n_new, co
  * position t and each visible entry j < (t+1)/m:
  *     scores[(b*n_q + i)*scores_stride + j] = sum_h w[h] * ReLU(q_idx[h] . key_j)
  * with key_j = idx_scale[row]*e4m3(idx_key[row]) (or the f32 key).
- *   q_idx [batch][n_q][heads_idx][d_idx] in q_dtype (CSA_BF16 or CSA_F32)
+ *   q_idx [batch][n_q][heads_idx][d_idx] in q_dtype (CSA_BF16, CSA_F32, or CSA_BF16_Q_E4M3:
+ *         bf16 values scored through their e4m3 quantisation, see the element types)
  *   w     f32 [batch][n_q][heads_idx]
  * Entries at or past the visible count are not written.
  */
@@ -204,6 +214,50 @@ CSA_API csa_status csa_sparse_attend(const csa_cache *cache, int batch, int n_q,
 CSA_API csa_status hca_attend(const csa_cache *cache, int batch, int n_q, const void *q, int q_dtype, int heads,
                       const float *sink, void *out, int out_dtype, float *out_lse, void *ws,
                       size_t ws_bytes, csa_stream_t stream);
+
+/*
+ * Sliding-window-only layer ([S] "Two kinds of memory instead of one": the
+ * multi-token-prediction block attends through the sliding window alone): the same
+ * shared-KV attention as hca_attend with no compressed entries -- the key set of a
+ * query at t is the window tokens max(0, t-n_win+1) .. t (rotated at their
+ * positions) plus the sink.  Such a layer's cache needs only its geometry (d,
+ * d_rope, n_win, win_cap, win_dtype, rope_theta), win and n_tokens; m, the entry
+ * storage and the indexer stream are ignored and may be NULL.
+ *   swa_append:  raw tokens x [batch][n_new][d] (in_dtype = win_dtype, 16-byte
+ *                aligned) go into the ring; n_tokens[b] += n_new.  No pooling.
+ *   swa_attend:  arguments and outputs as hca_attend; the workspace may be NULL
+ *                when swa_workspace_size returns 256 or less.
+ */
+CSA_API size_t swa_workspace_size(const csa_cache *cache, int batch, int n_q, int heads);
+CSA_API csa_status swa_append(const csa_cache *cache, int batch, int n_new, const void *x, int in_dtype,
+                              csa_stream_t stream);
+CSA_API csa_status swa_attend(const csa_cache *cache, int batch, int n_q, const void *q, int q_dtype, int heads,
+                              const float *sink, void *out, int out_dtype, float *out_lse, void *ws,
+                              size_t ws_bytes, csa_stream_t stream);
+
+/*
+ * Prefill of a long prompt in chunks ([E] "Practical Applications": processing
+ * million-token inputs): for every sequence b and every chunk of `chunk` new tokens,
+ * in order, csa_compress appends the chunk, csa_index_topk selects k entries for
+ * each of its queries and csa_sparse_attend attends -- each query sees exactly what
+ * a one-shot prefill of all n_new tokens would let it see, and every query row is
+ * computed the same way, so the result does not depend on the chunk length.
+ * Inputs are [batch][n_new][...] as in the calls above: x, gate [..][d] and idx_x,
+ * idx_gate [..][d_idx] in in_dtype; q_idx [..][heads_idx][d_idx] in q_idx_dtype;
+ * w f32 [..][heads_idx]; q [..][heads][d] in q_dtype; out [..][heads][d] in
+ * out_dtype; out_lse f32 [..][heads] or NULL.  win_cap >= n_win + chunk - 1.
+ * The workspace (csa_prefill_workspace_size bytes for this chunk length, 256-byte
+ * aligned) holds the calls' scratch -- its status word first -- and the chunk's
+ * selected indices.  The calls are launched on `stream` in order; none synchronises.
+ */
+CSA_API size_t csa_prefill_workspace_size(const csa_cache *cache, int chunk, int heads, int k);
+CSA_API csa_status csa_prefill_chunked(const csa_cache *cache, int batch, int n_new, int chunk, const void *x,
+                                       const void *gate, const void *idx_x, const void *idx_gate,
+                                       const float *pos_bias, const float *idx_pos_bias, int in_dtype,
+                                       const void *q_idx, int q_idx_dtype, const float *w, int heads_idx,
+                                       const void *q, int q_dtype, int heads, const float *sink, int k, void *out,
+                                       int out_dtype, float *out_lse, void *ws, size_t ws_bytes,
+                                       csa_stream_t stream);
 
 /*
  * csa_index_topk without a workspace argument, for callers that cannot allocate

@@ -18,14 +18,15 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libcsa.so")
 
-CSA_F32, CSA_BF16, CSA_E4M3 = 0, 1, 2
+CSA_F32, CSA_BF16, CSA_E4M3, CSA_BF16_Q_E4M3 = 0, 1, 2, 3
 CSA_OK = 0
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "WORKSPACE", 4: "CUDA", 5: "TIMEOUT"}
 STATUS_CODES = {v: k for k, v in STATUS_NAMES.items()}
 
 EXPORTS = ("csa_version", "csa_last_error", "csa_workspace_size", "csa_compress", "csa_index_scores", "csa_topk",
            "csa_index_topk", "csa_sparse_attend", "hca_attend", "csa_device_status", "csa_index_topk_static",
-           "csa_static_status", "csa_debug_set")
+           "csa_static_status", "csa_debug_set", "swa_workspace_size", "swa_append", "swa_attend",
+           "csa_prefill_workspace_size", "csa_prefill_chunked")
 CSA_DEBUG_WAIT_LIMIT, CSA_DEBUG_STARVE_INDEXER = 1, 2
 STATIC_SCRATCH_BYTES = 8 << 20
 
@@ -68,9 +69,17 @@ def lib() -> ctypes.CDLL:
         L.hca_attend.argtypes = [C, I, I, P, I, I, P, P, I, P, P, SZ, P]
         L.csa_device_status.argtypes = [P, ctypes.POINTER(I), P]
         L.csa_static_status.argtypes = [ctypes.POINTER(I), P]
+        L.swa_workspace_size.argtypes = [C, I, I, I]
+        L.swa_workspace_size.restype = SZ
+        L.swa_append.argtypes = [C, I, I, P, I, P]
+        L.swa_attend.argtypes = [C, I, I, P, I, I, P, P, I, P, P, SZ, P]
+        L.csa_prefill_workspace_size.argtypes = [C, I, I, I]
+        L.csa_prefill_workspace_size.restype = SZ
+        L.csa_prefill_chunked.argtypes = [C, I, I, I, P, P, P, P, P, P, I, P, I, P, I, P, I, I, P, I, P, I, P, P, SZ, P]
         L.csa_debug_set.argtypes = [I, ctypes.c_longlong]
         for name in EXPORTS:
-            if name not in ("csa_version", "csa_last_error", "csa_workspace_size"):
+            if name not in ("csa_version", "csa_last_error", "csa_workspace_size", "swa_workspace_size",
+                            "csa_prefill_workspace_size"):
                 getattr(L, name).restype = I
         _lib = L
     return _lib
@@ -192,13 +201,21 @@ def csa_compress(cache: Cache, x, gate, pos_bias, idx_x=None, idx_gate=None, idx
     _check(st, "csa_compress")
 
 
-def csa_index_scores(cache: Cache, q_idx, w, scores, ws=None, stream=None):
+def _q_idx_code(q_idx, q_fp8):
+    """dtype code of the indexer query; q_fp8 selects the query-side FP8 variant (bf16 input)."""
+    if q_fp8:
+        _need(q_idx, torch.bfloat16, "q_idx (query-side FP8 variant)")
+        return CSA_BF16_Q_E4M3
+    return _dtype_code(q_idx)
+
+
+def csa_index_scores(cache: Cache, q_idx, w, scores, ws=None, stream=None, q_fp8=False):
     """scores [B*n_q, stride] fp32 <- sum_h w_h ReLU(q_h . k_j) for visible entries."""
     B, n_q, H_I = q_idx.shape[0], q_idx.shape[1], q_idx.shape[2]
     _need(w, torch.float32, "w")
     _need(scores, torch.float32, "scores")
     p, n = _ws(ws)
-    st = lib().csa_index_scores(cache.ref, B, n_q, _ptr(q_idx), _dtype_code(q_idx), _ptr(w), H_I, _ptr(scores),
+    st = lib().csa_index_scores(cache.ref, B, n_q, _ptr(q_idx), _q_idx_code(q_idx, q_fp8), _ptr(w), H_I, _ptr(scores),
                                 scores.shape[-1], p, n, _stream(stream))
     _check(st, "csa_index_scores")
 
@@ -213,13 +230,13 @@ def csa_topk(cache: Cache, scores, batch, n_q, k, out_idx, out_count, ws=None, s
     _check(st, "csa_topk")
 
 
-def csa_index_topk(cache: Cache, q_idx, w, k, out_idx, out_count, ws, stream=None):
+def csa_index_topk(cache: Cache, q_idx, w, k, out_idx, out_count, ws, stream=None, q_fp8=False):
     B, n_q, H_I = q_idx.shape[0], q_idx.shape[1], q_idx.shape[2]
     _need(w, torch.float32, "w")
     _need(out_idx, torch.int32, "out_idx")
     _need(out_count, torch.int32, "out_count")
     p, n = _ws(ws)
-    st = lib().csa_index_topk(cache.ref, B, n_q, _ptr(q_idx), _dtype_code(q_idx), _ptr(w), H_I, k, _ptr(out_idx),
+    st = lib().csa_index_topk(cache.ref, B, n_q, _ptr(q_idx), _q_idx_code(q_idx, q_fp8), _ptr(w), H_I, k, _ptr(out_idx),
                               _ptr(out_count), p, n, _stream(stream))
     _check(st, "csa_index_topk")
 
@@ -254,6 +271,55 @@ def hca_attend(cache: Cache, q, sink, out, out_lse=None, ws=None, stream=None):
     st = lib().hca_attend(cache.ref, B, n_q, _ptr(q), _dtype_code(q), H, _ptr(sink), _ptr(out), _dtype_code(out),
                           _ptr(out_lse), p, n, _stream(stream))
     _check(st, "hca_attend")
+
+
+def swa_append(cache: Cache, x, stream=None):
+    """Sliding-window-only layer: raw tokens x [B, n_new, d] into the ring (no pooling)."""
+    st = lib().swa_append(cache.ref, x.shape[0], x.shape[1], _ptr(x), _dtype_code(x), _stream(stream))
+    _check(st, "swa_append")
+
+
+def swa_workspace_size(cache: Cache, batch: int, n_q: int, heads: int) -> int:
+    n = lib().swa_workspace_size(cache.ref, batch, n_q, heads)
+    if n == 0:
+        raise RuntimeError("invalid cache geometry: " + lib().csa_last_error().decode())
+    return n
+
+
+def swa_attend(cache: Cache, q, sink, out, out_lse=None, ws=None, stream=None):
+    """Attention over the window tokens and the sink only (sliding-window-only layer)."""
+    B, n_q, H = q.shape[0], q.shape[1], q.shape[2]
+    _need(sink, torch.float32, "sink")
+    p, n = _ws(ws)
+    st = lib().swa_attend(cache.ref, B, n_q, _ptr(q), _dtype_code(q), H, _ptr(sink), _ptr(out), _dtype_code(out),
+                          _ptr(out_lse), p, n, _stream(stream))
+    _check(st, "swa_attend")
+
+
+def prefill_workspace_size(cache: Cache, chunk: int, heads: int, k: int) -> int:
+    n = lib().csa_prefill_workspace_size(cache.ref, chunk, heads, k)
+    if n == 0:
+        raise RuntimeError("invalid prefill geometry: " + lib().csa_last_error().decode())
+    return n
+
+
+def csa_prefill_chunked(cache: Cache, chunk, x, gate, pos_bias, idx_x, idx_gate, idx_pos_bias, q_idx, w, q, sink,
+                        k, out, out_lse=None, ws=None, stream=None, q_fp8=False):
+    """Prefill of x [B, n_new, d] (and the matching indexer stream, queries and outputs)
+    in chunks of `chunk` tokens per sequence."""
+    B, n_new = x.shape[0], x.shape[1]
+    _need(w, torch.float32, "w")
+    _need(sink, torch.float32, "sink")
+    if ws is None:
+        ws = torch.zeros(prefill_workspace_size(cache, min(chunk, n_new), q.shape[2], k), dtype=torch.uint8,
+                         device=x.device)
+    p, n = _ws(ws)
+    st = lib().csa_prefill_chunked(cache.ref, B, n_new, chunk, _ptr(x), _ptr(gate), _ptr(idx_x), _ptr(idx_gate),
+                                   _ptr(pos_bias), _ptr(idx_pos_bias), _dtype_code(x), _ptr(q_idx),
+                                   _q_idx_code(q_idx, q_fp8), _ptr(w), q_idx.shape[2], _ptr(q), _dtype_code(q),
+                                   q.shape[2], _ptr(sink), k, _ptr(out), _dtype_code(out), _ptr(out_lse), p, n,
+                                   _stream(stream))
+    _check(st, "csa_prefill_chunked")
 
 
 def device_status(ws: torch.Tensor, stream=None) -> int:

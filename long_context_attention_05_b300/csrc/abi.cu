@@ -132,10 +132,11 @@ struct AttendPlan {
   size_t part_o_bytes, part_ml_bytes;
 };
 
-AttendPlan attend_plan(const csa_cache *c, int batch, int n_q, int heads, long long list_cap) {
+// one_split: the prefill plan (one CTA walks all of a row's chunks) whatever n_q is
+AttendPlan attend_plan(const csa_cache *c, int batch, int n_q, int heads, long long list_cap, bool one_split = false) {
   AttendPlan p;
   p.tc = csa::attend_tc_supported(view(c), heads, CSA_BF16);
-  csa::attend_plan(n_q, list_cap, c->n_win, p.tc, p.n_splits, p.cps);
+  csa::attend_plan(one_split ? 2 : n_q, list_cap, c->n_win, p.tc, p.n_splits, p.cps);
   const size_t parts = (size_t)batch * n_q * p.n_splits * heads;
   p.part_o_bytes = p.n_splits > 1 ? align256(parts * c->d * sizeof(float)) : 0;
   p.part_ml_bytes = p.n_splits > 1 ? align256(parts * 2 * sizeof(float)) : 0;
@@ -170,9 +171,12 @@ csa_status check_q(int batch, int n_q, const csa_cache *c) {
   return ok();
 }
 
+// no_entries: a sliding-window-only layer -- the key list is the window alone (the
+// cache view's entry capacity is 0, so no entry is ever visible or read)
 csa_status attend_common(const csa_cache *c, int batch, int n_q, const void *q, int q_dtype, int heads,
                          const float *sink, const int32_t *idx, int k, void *out, int out_dtype, float *out_lse,
-                         void *ws, size_t ws_bytes, cudaStream_t st) {
+                         void *ws, size_t ws_bytes, cudaStream_t st, bool no_entries = false,
+                         bool one_split = false) {
   csa_status s = check_cache(c);
   if (s) return s;
   if ((s = check_q(batch, n_q, c))) return s;
@@ -184,12 +188,13 @@ csa_status attend_common(const csa_cache *c, int batch, int n_q, const void *q, 
   if (((uintptr_t)q & 15) || ((uintptr_t)out & 7) || ((uintptr_t)idx & 3) || ((uintptr_t)out_lse & 3))
     return fail(CSA_ERR_INVALID_ARG, "q must be 16-byte, out 8-byte, idx and out_lse 4-byte aligned");
   if (csa::attend_smem_bytes(c->d) > 227 * 1024) return fail(CSA_ERR_UNSUPPORTED, "d=%d too large", c->d);
-  const long long list_cap = idx ? (long long)k : entry_cap(c);
-  const AttendPlan p = attend_plan(c, batch, n_q, heads, list_cap);
+  const long long list_cap = no_entries ? 0 : idx ? (long long)k : entry_cap(c);
+  const AttendPlan p = attend_plan(c, batch, n_q, heads, list_cap, one_split);
   const size_t need = p.n_splits > 1 ? kHeader + p.part_o_bytes + p.part_ml_bytes : 0;
   if ((s = check_ws(ws, ws_bytes, need))) return s;
   csa::AttendArgs a;
   a.c = view(c);
+  if (no_entries) a.c.cap = 0;
   a.rope = rope_table(c->rope_theta, c->d_rope);
   a.n_q = n_q; a.heads = heads; a.q_dtype = q_dtype; a.out_dtype = out_dtype;
   a.q = (const uint8_t *)q; a.sink = sink; a.idx = idx; a.k = k;
@@ -211,7 +216,8 @@ csa_status check_index_args(const csa_cache *c, int batch, int n_q, const void *
   if (c->d_idx == 0) return fail(CSA_ERR_INVALID_ARG, "cache has no indexer stream (d_idx == 0)");
   if (heads_idx < 1 || heads_idx > 128) return fail(CSA_ERR_UNSUPPORTED, "heads_idx=%d outside [1,128]", heads_idx);
   if (!q_idx || !w) return fail(CSA_ERR_INVALID_ARG, "q_idx and w must be non-NULL");
-  if (q_dtype != CSA_BF16 && q_dtype != CSA_F32) return fail(CSA_ERR_INVALID_ARG, "q_dtype must be BF16 or F32");
+  if (q_dtype != CSA_BF16 && q_dtype != CSA_F32 && q_dtype != CSA_BF16_Q_E4M3)
+    return fail(CSA_ERR_INVALID_ARG, "q_dtype must be BF16, F32 or BF16_Q_E4M3");
   if ((size_t)heads_idx * (c->d_idx + 1) * sizeof(float) > 227 * 1024)
     return fail(CSA_ERR_UNSUPPORTED, "indexer query too large");
   return ok();
@@ -233,6 +239,45 @@ cudaError_t launch_indexer(const csa_cache *c, int batch, int n_q, const void *q
                                 ws ? (int *)ws : nullptr, hist, dbg, st);
   }
   return csa::launch_index_generic(v, batch, n_q, q_idx, q_dtype, w, heads_idx, scores, stride, entry_cap(c), st);
+}
+
+}  // namespace
+
+namespace {
+
+// A sliding-window-only layer's cache as the attention path sees it: the window ring
+// and the token counts; m, the entry storage and the indexer stream are ignored (the
+// entry fields get stand-ins that are never read: the entry capacity is 0).
+csa_status swa_view(const csa_cache *c, csa_cache &cc) {
+  if (!c) return fail(CSA_ERR_INVALID_ARG, "cache is NULL");
+  if (!c->win || !c->n_tokens) return fail(CSA_ERR_INVALID_ARG, "win and n_tokens must be non-NULL");
+  cc = *c;
+  cc.m = 1; cc.d_idx = 0; cc.page_size = 0; cc.max_pages = 0; cc.max_entries = 1;
+  cc.kv_dtype = c->win_dtype == CSA_BF16 ? CSA_E4M3 : CSA_F32;
+  cc.kv_nope = c->win; cc.kv_rope = c->win; cc.kv_scale = reinterpret_cast<float *>(c->win);
+  cc.idx_key = nullptr; cc.idx_scale = nullptr; cc.page_table = nullptr;
+  cc.pool_state = reinterpret_cast<float *>(c->win);
+  return check_cache(&cc);
+}
+
+// Sequence b of a cache as a cache of one sequence (pointer offsets only).
+csa_cache seq_view(const csa_cache *c, int b) {
+  csa_cache s = *c;
+  const size_t eb = c->kv_dtype == CSA_E4M3 ? 1 : 4;   // bytes per non-rotary / indexer-key element
+  if (c->page_size == 0) {
+    const size_t r0 = (size_t)b * (size_t)c->max_entries;
+    s.kv_nope = (uint8_t *)c->kv_nope + r0 * (c->d - c->d_rope) * eb;
+    s.kv_rope = (uint8_t *)c->kv_rope + r0 * c->d_rope * (c->kv_dtype == CSA_E4M3 ? 2 : 4);
+    if (c->kv_scale) s.kv_scale = c->kv_scale + r0;
+    if (c->idx_key) s.idx_key = (uint8_t *)c->idx_key + r0 * c->d_idx * eb;
+    if (c->idx_scale) s.idx_scale = c->idx_scale + r0;
+  } else {
+    s.page_table = c->page_table + (size_t)b * c->max_pages;
+  }
+  s.win = (uint8_t *)c->win + (size_t)b * c->win_cap * c->d * (c->win_dtype == CSA_F32 ? 4 : 2);
+  s.pool_state = c->pool_state + (size_t)b * 3 * (c->d + c->d_idx);
+  s.n_tokens = c->n_tokens + b;
+  return s;
 }
 
 }  // namespace
@@ -394,6 +439,94 @@ csa_status hca_attend(const csa_cache *c, int batch, int n_q, const void *q, int
                       csa_stream_t stream) {
   return attend_common(c, batch, n_q, q, q_dtype, heads, sink, nullptr, 0, out, out_dtype, out_lse, ws, ws_bytes,
                        (cudaStream_t)stream);
+}
+
+size_t swa_workspace_size(const csa_cache *c, int batch, int n_q, int heads) {
+  csa_cache cc;
+  if (swa_view(c, cc) || batch < 1 || n_q < 1 || heads < 1) return 0;
+  const AttendPlan p = attend_plan(&cc, batch, n_q, heads, 0);
+  return kHeader + p.part_o_bytes + p.part_ml_bytes;
+}
+
+csa_status swa_append(const csa_cache *c, int batch, int n_new, const void *x, int in_dtype, csa_stream_t stream) {
+  csa_cache cc;
+  csa_status s = swa_view(c, cc);
+  if (s) return s;
+  if (batch < 1 || n_new < 1) return fail(CSA_ERR_INVALID_ARG, "batch=%d n_new=%d must be >= 1", batch, n_new);
+  if (in_dtype != c->win_dtype) return fail(CSA_ERR_INVALID_ARG, "in_dtype must equal the ring dtype");
+  if (!x || ((uintptr_t)x & 15)) return fail(CSA_ERR_INVALID_ARG, "x must be non-NULL and 16-byte aligned");
+  return cuda_status(csa::launch_swa_append(view(&cc), batch, n_new, in_dtype, x, (cudaStream_t)stream),
+                     "window append launch");
+}
+
+csa_status swa_attend(const csa_cache *c, int batch, int n_q, const void *q, int q_dtype, int heads, const float *sink,
+                      void *out, int out_dtype, float *out_lse, void *ws, size_t ws_bytes, csa_stream_t stream) {
+  csa_cache cc;
+  csa_status s = swa_view(c, cc);
+  if (s) return s;
+  return attend_common(&cc, batch, n_q, q, q_dtype, heads, sink, nullptr, 0, out, out_dtype, out_lse, ws, ws_bytes,
+                       (cudaStream_t)stream, true);
+}
+
+// Workspace of the calls one chunk of at most `chunk` rows makes: the largest over the
+// chunk lengths a call can see (the prefix histograms are reserved only for calls of
+// at most kPrefixRowsMax rows, so the size is not monotone in the rows).
+static size_t prefill_inner(const csa_cache *c, int chunk, int heads, int k) {
+  const csa_cache s = seq_view(c, 0);
+  const size_t a = csa_workspace_size(&s, 1, chunk, heads, k);
+  const size_t b = csa_workspace_size(&s, 1, std::min(chunk, csa::kPrefixRowsMax), heads, k);
+  return (a == 0 || b == 0) ? 0 : align256(std::max(a, b));
+}
+
+size_t csa_prefill_workspace_size(const csa_cache *c, int chunk, int heads, int k) {
+  if (check_cache(c) || chunk < 1 || heads < 1 || k < 1) return 0;
+  const size_t inner = prefill_inner(c, chunk, heads, k);
+  if (inner == 0) return 0;
+  return inner + align256((size_t)chunk * k * sizeof(int32_t)) + align256((size_t)chunk * sizeof(int32_t));
+}
+
+csa_status csa_prefill_chunked(const csa_cache *c, int batch, int n_new, int chunk, const void *x, const void *gate,
+                               const void *idx_x, const void *idx_gate, const float *pos_bias,
+                               const float *idx_pos_bias, int in_dtype, const void *q_idx, int q_idx_dtype,
+                               const float *w, int heads_idx, const void *q, int q_dtype, int heads,
+                               const float *sink, int k, void *out, int out_dtype, float *out_lse, void *ws,
+                               size_t ws_bytes, csa_stream_t stream) {
+  csa_status s = check_cache(c);
+  if (s) return s;
+  if (batch < 1 || n_new < 1 || chunk < 1) return fail(CSA_ERR_INVALID_ARG, "batch, n_new and chunk must be >= 1");
+  if (c->d_idx == 0) return fail(CSA_ERR_INVALID_ARG, "cache has no indexer stream (d_idx == 0)");
+  if (!x || !gate || !idx_x || !idx_gate || !q_idx || !w || !q || !sink || !out)
+    return fail(CSA_ERR_INVALID_ARG, "NULL input or output pointer");
+  const size_t need = csa_prefill_workspace_size(c, std::min(chunk, n_new), heads, k);
+  if (need == 0) return fail(CSA_ERR_INVALID_ARG, "invalid prefill geometry");
+  if ((s = check_ws(ws, ws_bytes, need))) return s;
+  const int L0 = std::min(chunk, n_new);
+  const size_t inner = prefill_inner(c, L0, heads, k);
+  int32_t *idx = (int32_t *)((char *)ws + inner);
+  int32_t *cnt = (int32_t *)((char *)ws + inner + align256((size_t)L0 * k * sizeof(int32_t)));
+  const size_t tb = in_dtype == CSA_F32 ? 4 : 2, qb = q_dtype == CSA_F32 ? 4 : 2;
+  const size_t qib = q_idx_dtype == CSA_F32 ? 4 : 2, ob = out_dtype == CSA_F32 ? 4 : 2;
+  for (int b = 0; b < batch; ++b) {
+    const csa_cache sc = seq_view(c, b);
+    for (int p0 = 0; p0 < n_new; p0 += chunk) {
+      const int L = std::min(chunk, n_new - p0);
+      const size_t r0 = (size_t)b * n_new + p0;   // first row of this chunk in the [batch][n_new] inputs
+      const size_t inner_l = csa_workspace_size(&sc, 1, L, heads, k);
+      s = csa_compress(&sc, 1, L, (const char *)x + r0 * c->d * tb, (const char *)gate + r0 * c->d * tb,
+                       (const char *)idx_x + r0 * c->d_idx * tb, (const char *)idx_gate + r0 * c->d_idx * tb,
+                       pos_bias, idx_pos_bias, in_dtype, stream);
+      if (s) return s;
+      s = csa_index_topk(&sc, 1, L, (const char *)q_idx + r0 * heads_idx * c->d_idx * qib, q_idx_dtype,
+                         w + r0 * heads_idx, heads_idx, k, idx, cnt, ws, inner_l, stream);
+      if (s) return s;
+      // every chunk takes the prefill plan (a one-token chunk too): each row is computed alike
+      s = attend_common(&sc, 1, L, (const char *)q + r0 * heads * c->d * qb, q_dtype, heads, sink, idx, k,
+                        (char *)out + r0 * heads * c->d * ob, out_dtype, out_lse ? out_lse + r0 * heads : nullptr,
+                        ws, inner_l, (cudaStream_t)stream, false, true);
+      if (s) return s;
+    }
+  }
+  return ok();
 }
 
 csa_status csa_static_status(int *status, csa_stream_t stream) {

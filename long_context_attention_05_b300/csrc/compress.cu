@@ -165,6 +165,32 @@ __global__ void __launch_bounds__(1024) k_compress(CompressArgs a) {
   }
 }
 
+// Sliding-window-only layer: the raw tokens go into the window ring (the last win_cap
+// of them) and n_tokens advances; nothing is pooled.  One CTA per sequence reads
+// n_tokens first and advances it after every copy of the sequence is issued.
+__global__ void __launch_bounds__(256) k_swa_append(CacheView c, int n_new, int in_dtype, const uint8_t *x) {
+  const int b = blockIdx.x;
+  pdl_wait();      // the previous step's attention reads the ring and n_tokens
+  pdl_trigger();
+  __shared__ long long sh_n0;
+  if (threadIdx.x == 0) sh_n0 = c.n_tokens[b];
+  __syncthreads();
+  const long long n0 = sh_n0;
+  const long long first = max(0LL, (long long)n_new - c.win_cap);   // earlier tokens would be overwritten
+  const int esz = in_dtype == CSA_F32 ? 4 : 2;
+  const long long row_bytes = (long long)c.d * esz;                 // a multiple of 16 (d % 16 == 0)
+  const long long n_vec = (n_new - first) * (row_bytes / 16);
+  uint8_t *ring = const_cast<uint8_t *>(c.win);
+  for (long long v = threadIdx.x; v < n_vec; v += blockDim.x) {
+    const long long i = first + v / (row_bytes / 16), piece = v % (row_bytes / 16);
+    const long long p = n0 + i;
+    const uint4 val = __ldg(reinterpret_cast<const uint4 *>(x + ((long long)b * n_new + i) * row_bytes) + piece);
+    reinterpret_cast<uint4 *>(ring + ((long long)b * c.win_cap + p % c.win_cap) * row_bytes)[piece] = val;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) c.n_tokens[b] = n0 + n_new;
+}
+
 __global__ void k_advance(long long *n_tokens, int batch, int n_new) {
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b < batch) n_tokens[b] += n_new;
@@ -185,6 +211,10 @@ cudaError_t launch_compress(const CacheView &c, const RopeTable &rope, int batch
   if (e != cudaSuccess || n_new == 1) return e;
   k_advance<<<(batch + 127) / 128, 128, 0, st>>>(c.n_tokens, batch, n_new);
   return cudaGetLastError();
+}
+
+cudaError_t launch_swa_append(const CacheView &c, int batch, int n_new, int in_dtype, const void *x, cudaStream_t st) {
+  return launch_pdl(k_swa_append, dim3(batch), dim3(256), 0, st, 1, c, n_new, in_dtype, (const uint8_t *)x);
 }
 
 }  // namespace csa

@@ -38,6 +38,17 @@ __global__ void __launch_bounds__(256) k_index_generic(CacheView c, int n_q, con
     qs[e] = load_tok(q_idx, q_dtype, (long long)row * heads_idx * DI + e);
   for (int e = threadIdx.x; e < heads_idx; e += blockDim.x) ws[e] = w[(long long)row * heads_idx + e];
   __syncthreads();
+  if (q_dtype == CSA_BF16_Q_E4M3) {   // query-side FP8: each head's vector on the e4m3 grid of a power-of-two scale
+    for (int h = threadIdx.x; h < heads_idx; h += blockDim.x) {
+      float am = 0.f;
+      for (int e = 0; e < DI; ++e) am = fmaxf(am, fabsf(qs[h * DI + e]));
+      int ex = 0;
+      frexpf(am, &ex);
+      const float S = am > 0.f ? ldexpf(1.f, 8 - ex) : 1.f, inv = am > 0.f ? ldexpf(1.f, ex - 8) : 1.f;
+      for (int e = 0; e < DI; ++e) qs[h * DI + e] = e4m3_to_f32(f32_to_e4m3_rn_sat(qs[h * DI + e] * S)) * inv;
+    }
+    __syncthreads();
+  }
   if (j >= n_vis) return;
   const long long r = entry_row(c, b, j);
   float k[DI];

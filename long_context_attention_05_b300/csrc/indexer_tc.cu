@@ -64,6 +64,7 @@ struct TcArgs {
   long long wait_limit;   // polls before a bounded wait gives up
   int starve;         // failure injection for tests: the producer issues no key copies
   int q_vec;          // q_idx is 16-byte aligned: vector loads of the query
+  int hi_only;        // query-side FP8 variant: one e4m3 operand (N = heads), no lo term
   unsigned *hist;     // per-row histograms of score-key prefixes (kPrefixBins each), or null
 };
 
@@ -347,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
       for (int e = 0; e < 4; ++e) {
         const float x = v[e] * S;
         const uint8_t hi = f32_to_e4m3_rn_sat(x);
-        const uint8_t lo = f32_to_e4m3_rn_sat((x - e4m3_to_f32(hi)) * 16.f);
+        const uint8_t lo = a.hi_only ? (uint8_t)0 : f32_to_e4m3_rn_sat((x - e4m3_to_f32(hi)) * 16.f);
         hw |= (uint32_t)hi << (8 * e);
         lw |= (uint32_t)lo << (8 * e);
       }
@@ -417,7 +418,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
   } else if (warp == 1) {
     if (lane == 0) {   // ---- MMA issuer
       // one MMA per K step: N = 2H columns, hi heads in [0, H), lo heads in [H, 2H)
-      const uint32_t idesc = (1u << 4) | ((uint32_t)((2 * H) >> 3) << 17) | ((uint32_t)(kTileM >> 4) << 24);
+      const int n_mma = a.hi_only ? H : 2 * H;   // hi only, or hi | lo
+      const uint32_t idesc = (1u << 4) | ((uint32_t)(n_mma >> 3) << 17) | ((uint32_t)(kTileM >> 4) << 24);
       const uint32_t bh = su32(bhi);
       for (int it = 0; it < n_it; ++it) {
         const int s = it % kStages;
@@ -486,7 +488,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
         for (int c0 = 0; c0 < H; c0 += 32) {
           uint32_t hv[32], lv[32];
           tmem_ld32(taddr + c0, hv);
-          tmem_ld32(taddr + H + c0, lv);
+          if (a.hi_only) {
+#pragma unroll
+            for (int q = 0; q < 32; ++q) lv[q] = 0u;
+          } else {
+            tmem_ld32(taddr + H + c0, lv);
+          }
           tmem_wait_ld();
           // w_h/S_h as 16-byte shared loads: a quarter of the shared-memory wavefronts of
           // scalar loads (shared-memory bandwidth is shared with the TMA writes and MMA reads)
@@ -602,6 +609,8 @@ cudaError_t launch_index_tc(const CacheView &c, int batch, int n_q, const void *
   a.wait_limit = dbg.wait_limit > 0 ? dbg.wait_limit : (1LL << 24);
   a.starve = dbg.starve;
   a.q_vec = ((uintptr_t)q_idx & 15) == 0;
+  a.hi_only = q_dtype == CSA_BF16_Q_E4M3;
+  if (a.hi_only) a.q_dtype = CSA_BF16;   // the input is bf16 either way
   a.hist = hist;
   const int rows_q = batch * n_q;
   a.rows = rows_q;

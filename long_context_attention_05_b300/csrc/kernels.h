@@ -38,6 +38,8 @@ cudaError_t launch_compress(const CacheView &c, const RopeTable &rope, int batch
                             const void *x, const void *gate, const void *ix, const void *ig,
                             const float *pb, const float *ipb, cudaStream_t st);
 
+cudaError_t launch_swa_append(const CacheView &c, int batch, int n_new, int in_dtype, const void *x, cudaStream_t st);
+
 cudaError_t launch_index_generic(const CacheView &c, int batch, int n_q, const void *q_idx, int q_dtype,
                                  const float *w, int heads_idx, float *scores, long long stride,
                                  long long n_cap, cudaStream_t st);

@@ -94,6 +94,7 @@ class Workload:
     theta: float = 10000.0
     extra_entries: int = 64     # spare entry capacity per sequence for repeated steps
     spare_pages: int = 0        # spare physical pages in the pool (paged caches)
+    q_fp8: bool = False         # indexer: query-side FP8 variant
 
     def __post_init__(self):
         if len(self.ctx) != self.batch:

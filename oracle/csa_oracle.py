@@ -256,6 +256,24 @@ def visible_entries(t: int, m: int) -> int:
     return (t + 1) // m
 
 
+def quantise_query_e4m3(q_idx: np.ndarray) -> np.ndarray:
+    """Query-side FP8 variant of the indexer (the write-ups call the indexer low
+    precision; [S]): each head's query vector q_h is put on the e4m3 grid of a
+    power-of-two scale S_h with max|q_h| * S_h in [2^7, 2^8) (RNE), and the scores
+    use q_h' = e4m3(q_h * S_h) / S_h.  A zero vector stays zero.  (The power-of-two
+    scale is this library's reading: multiplying by it is exact.)"""
+    q = np.asarray(q_idx, np.float64)
+    out = np.zeros_like(q)
+    for h in range(q.shape[0]):
+        amax = np.abs(q[h]).max() if q.shape[1] else 0.0
+        if amax == 0:
+            continue
+        _, ex = math.frexp(amax)          # amax = f * 2^ex, f in [0.5, 1)
+        s = 2.0 ** (8 - ex)
+        out[h] = decode_e4m3(encode_e4m3(q[h] * s)) / s
+    return out
+
+
 def indexer_scores(q_idx: np.ndarray, w: np.ndarray, keys: np.ndarray) -> np.ndarray:
     """score_j = sum_h w_h * ReLU(q_h . k_j).  q_idx [H_I, d_I], w [H_I], keys [N, d_I]."""
     dots = keys @ np.asarray(q_idx, np.float64).T          # [N, H_I]
@@ -312,21 +330,24 @@ def ring_slot(pos: np.ndarray, win_cap: int) -> np.ndarray:
 def query_step(kind: str, q: np.ndarray, t: int, sink: np.ndarray, entries: np.ndarray, window_fn,
                m: int, n_win: int, d_rope: int, theta: float, q_idx: Optional[np.ndarray] = None,
                w_idx: Optional[np.ndarray] = None, idx_keys: Optional[np.ndarray] = None,
-               k: int = 0, idx_override: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
+               k: int = 0, idx_override: Optional[np.ndarray] = None, q_fp8: bool = False
+               ) -> Dict[str, np.ndarray]:
     """All stages for the query at position t of one sequence.
 
     entries / idx_keys: float64 decoded stored entries / indexer keys of the
     sequence (at least the visible ones); window_fn(positions) -> raw float64
     window tokens.  CSA: indexer scores over the visible entries, top-k, then
     attention over the selected entries + window + sink.  HCA: attention over
-    all visible entries + window + sink.  idx_override replaces the oracle's own
+    all visible entries + window + sink.  SWA (sliding-window-only layer, [S]: the
+    multi-token-prediction block): window + sink, no entries.  idx_override replaces the oracle's own
     top-k set in the attention stage (used to test attention on a given set).
+    q_fp8 scores with the query-side FP8 variant (quantise_query_e4m3).
     """
-    n_vis = visible_entries(t, m)
+    n_vis = visible_entries(t, m) if kind != "swa" else 0
     assert entries.shape[0] >= n_vis, "entries missing"
     res: Dict[str, np.ndarray] = {"n_vis": n_vis}
     if kind == "csa":
-        scores = indexer_scores(q_idx, w_idx, idx_keys[:n_vis])
+        scores = indexer_scores(quantise_query_e4m3(q_idx) if q_fp8 else q_idx, w_idx, idx_keys[:n_vis])
         idx, count = topk(scores, k)
         res.update(scores=scores, idx=idx, count=count)
         use = idx_override if idx_override is not None else idx

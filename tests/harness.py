@@ -122,7 +122,7 @@ def oracle_seeded_step(w, arrs, inp, b, i, idx_override=None, ent_cache=None):
     kw = {}
     if w.kind == "csa":
         kw = dict(q_idx=_dec_tok(inp["q_idx"][b, i], w), w_idx=inp["w_idx"][b, i].astype(np.float64),
-                  idx_keys=keys, k=w.k, idx_override=idx_override)
+                  idx_keys=keys, k=w.k, idx_override=idx_override, q_fp8=w.q_fp8)
     res = O.query_step(w.kind, q, t, inp["sink"].astype(np.float64), ent, window_fn(w, arrs, inp, b, ctx), w.m,
                        w.n_win, w.d_rope, w.theta, **kw)
     res["n_old"] = n_old
@@ -228,10 +228,10 @@ def gpu_query_stages(w, cache, gi, out_dtype, ws, chained=False, idx_in=None):
         idx = torch.full((B, n_q, w.k), -7, dtype=torch.int32, device="cuda")
         cnt = torch.full((B, n_q), -7, dtype=torch.int32, device="cuda")
         if chained:
-            L.csa_index_topk(cache, gi["q_idx"], gi["w_idx"], w.k, idx, cnt, ws)
+            L.csa_index_topk(cache, gi["q_idx"], gi["w_idx"], w.k, idx, cnt, ws, q_fp8=w.q_fp8)
         else:
             scores = torch.full((B * n_q, cache.entry_cap), float("nan"), dtype=torch.float32, device="cuda")
-            L.csa_index_scores(cache, gi["q_idx"], gi["w_idx"], scores, ws)
+            L.csa_index_scores(cache, gi["q_idx"], gi["w_idx"], scores, ws, q_fp8=w.q_fp8)
             L.csa_topk(cache, scores, B, n_q, w.k, idx, cnt, ws)
             res["scores"] = scores
         use = idx if idx_in is None else idx_in

@@ -430,3 +430,55 @@ def test_query_step_brute_force_tiny():
         assert abs(res["lse"][h] - math.log(den)) < 1e-12
     assert res["idx"].tolist() == sorted(order) and res["count"] == k
     assert np.allclose(res["scores"], sc, rtol=0, atol=1e-12)
+
+
+def test_query_side_fp8_quantiser_hand_values():
+    """The query-side FP8 variant: per head, the power of two S with max|q_h| S in
+    [2^7, 2^8), then e4m3 rounding to nearest even.  q_h = (1, -0.3, 0, 0.01): S = 128,
+    q S = (128, -38.4, 0, 1.28) -> e4m3 (128, -40, 0, 1.25) -> q' = (1, -0.3125, 0, 0.009765625)."""
+    q = np.array([[1.0, -0.3, 0.0, 0.01],
+                  [0.0, 0.0, 0.0, 0.0],
+                  [-6.0, 3.0, 0.5, 2.5]])
+    got = O.quantise_query_e4m3(q)
+    assert got[0].tolist() == [1.0, -0.3125, 0.0, 1.25 / 128]
+    assert not got[1].any()
+    # head 2: max 6 -> S = 2^(8-3) = 32: 6*32 = 192 (exact), 96, 16, 80 -> all on the grid
+    assert got[2].tolist() == [-6.0, 3.0, 0.5, 2.5]
+    # every head lands on its scale's e4m3 grid, within half a step of q
+    r = rng.standard_normal((8, 64)) * np.exp(rng.uniform(-8, 8, (8, 1)))
+    qq = O.quantise_query_e4m3(r)
+    for h in range(8):
+        _, ex = math.frexp(np.abs(r[h]).max())
+        s = 2.0 ** (8 - ex)
+        assert 128 <= np.abs(r[h]).max() * s < 256
+        codes = O.encode_e4m3(qq[h] * s)
+        assert np.array_equal(O.decode_e4m3(codes), qq[h] * s)
+        assert np.all(np.abs(qq[h] - r[h]) <= np.abs(r[h]) * 2.0 ** -4 + 2.0 ** -10 / s)
+
+
+def test_window_only_layer_brute_force_and_relation_to_hca():
+    """A sliding-window-only query: one softmax over the window tokens (rotated at their
+    positions) and the sink, no entries -- written out with loops; and equal to HCA's
+    result for a query that sees no complete block yet."""
+    d, dr, n_win, theta = 4, 2, 3, 10000.0
+    q = rng.standard_normal((2, d))
+    sink = np.array([0.2, -0.4])
+    raw = {p: rng.standard_normal(d) for p in range(12)}
+    wf = lambda pos: np.array([raw[int(p)] for p in pos])
+
+    def turn(v, p):
+        return np.array([v[0], v[1], v[2] * math.cos(p) - v[3] * math.sin(p), v[2] * math.sin(p) + v[3] * math.cos(p)])
+
+    for t in (0, 1, 11):
+        res = O.query_step("swa", q, t, sink, np.zeros((0, d)), wf, 128, n_win, dr, theta)
+        kv = [turn(raw[p], p) for p in range(max(0, t - n_win + 1), t + 1)]
+        for h in range(2):
+            qh = turn(q[h], t)
+            lg = [float(qh @ v) / math.sqrt(d) for v in kv]
+            den = sum(math.exp(x) for x in lg) + math.exp(sink[h])
+            o = sum(math.exp(x) / den * v for x, v in zip(lg, kv))
+            assert np.allclose(res["o"][h], o, rtol=0, atol=1e-12) and abs(res["lse"][h] - math.log(den)) < 1e-12
+    ent = rng.standard_normal((5, d))
+    a = O.query_step("swa", q, 2, sink, ent, wf, 4, n_win, dr, theta)
+    b = O.query_step("hca", q, 2, sink, ent, wf, 4, n_win, dr, theta)     # t = 2 < m - 1: no entry visible
+    assert np.array_equal(a["o"], b["o"]) and np.array_equal(a["lse"], b["lse"])

@@ -256,3 +256,23 @@ def test_topk_very_long_rows_take_the_global_memory_path():
     arrs, inp = _seeded(w)
     res = H.gpu_seeded_step(w, arrs, inp)
     _check_step(w, arrs, inp, res, H.TOL_LOW, what="2M ctx")
+
+
+@pytest.mark.parametrize("heads_idx", [64, 48])
+def test_indexer_query_side_fp8_variant(heads_idx):
+    """The query-side FP8 indexer (64 heads: tensor-core kernel with one e4m3 operand;
+    48 heads: CUDA-core kernel) against the oracle's mirror of the same quantisation,
+    through the separate calls (scores compared) and the fused call; and the variant
+    really changes the scores relative to the exact bf16 query."""
+    import dataclasses
+    w = S.config2(ctx=(8192, 20000, 4096, 131072), heads_idx=heads_idx, k=512, q_fp8=True)
+    arrs, inp = _seeded(w)
+    res = H.gpu_seeded_step(w, arrs, inp)
+    refs = {}
+    _check_step(w, arrs, inp, res, H.TOL_LOW, what=f"q fp8 h={heads_idx}", refs=refs)
+    fused = H.gpu_seeded_step(w, arrs, inp, chained=True)
+    assert np.array_equal(fused["idx"], res["idx"]) and np.array_equal(fused["o"], res["o"])
+    exact = H.gpu_seeded_step(dataclasses.replace(w, q_fp8=False), arrs, inp)
+    n = w.n_entries[3]
+    rel = np.abs(exact["scores"][3, :n] - res["scores"][3, :n]).max() / np.abs(exact["scores"][3, :n]).max()
+    assert rel > 1e-4, rel
