@@ -28,7 +28,7 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-WORKLOADS = ("csa_decode_1m", "hca_decode_128k", "stack_decode_paged", "csa_prefill_8k")
+WORKLOADS = ("csa_decode_1m", "csa_decode_1m_fp4", "hca_decode_128k", "stack_decode_paged", "csa_prefill_8k")
 
 
 def _peaks():
@@ -182,6 +182,8 @@ def _workload(name, steps_total):
     extra = steps_total // 4 + 16
     if name == "csa_decode_1m":
         return [S.config2(extra_entries=extra)]
+    if name == "csa_decode_1m_fp4":   # the same step with FP4 (e2m1) indexer keys
+        return [S.config2(extra_entries=extra, idx_dtype="e2m1", name="csa_decode_1m_fp4")]
     if name == "hca_decode_128k":
         return [S.config1(extra_entries=extra)]
     if name == "stack_decode_paged":
@@ -202,7 +204,7 @@ def _alg_bytes(w):
     new_tok = B * nq * 2 * (w.d + w.d_idx) * tok
     win = B * nq * w.n_win * w.d * tok
     if w.kind == "csa":
-        key = w.d_idx + 4 if w.kv_dtype == "e4m3" else 4 * w.d_idx
+        key = (w.d_idx // 2 + 4) if w.idx_dtype == "e2m1" else (w.d_idx + 4 if w.kv_dtype == "e4m3" else 4 * w.d_idx)
         idx_bytes = int(n_e.sum()) * nq * key + B * nq * w.heads_idx * (w.d_idx * tok + 4)
         att = B * nq * w.k * entry
     else:
@@ -328,7 +330,9 @@ def config_dict(wl, workload):
     w0l = wl[0]
     return {"workload": w0l.name if len(wl) == 1 else workload, "batch_per_gpu": w0l.batch,
             "ctx_tokens": int(max(w0l.ctx)), "entries_per_seq": int(max(w0l.n_entries)), "m": w0l.m,
-            "heads": w0l.heads, "d": w0l.d, "indexer": f"{w0l.heads_idx}x{w0l.d_idx} e4m3", "top_k": w0l.k,
+            "heads": w0l.heads, "d": w0l.d,
+            "indexer": f"{w0l.heads_idx}x{w0l.d_idx} {w0l.idx_dtype or 'e4m3'}" if w0l.kind == "csa" else None,
+            "top_k": w0l.k,
             "window": w0l.n_win, "layers": len(wl), "new_tokens_per_seq": w0l.n_new,
             "l2": "inputs larger than L2 (cache >> 126 MB)"}
 

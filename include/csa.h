@@ -72,7 +72,7 @@ enum {
  * scores with q_h' = e4m3(q_h * S) / S.  The default (CSA_BF16) scores with the
  * bf16 query itself.
  */
-enum { CSA_F32 = 0, CSA_BF16 = 1, CSA_E4M3 = 2, CSA_BF16_Q_E4M3 = 3 };
+enum { CSA_F32 = 0, CSA_BF16 = 1, CSA_E4M3 = 2, CSA_BF16_Q_E4M3 = 3, CSA_E2M1 = 4 };
 
 /*
  * One layer's compressed cache.  Geometry fields are host values; pointers are
@@ -87,6 +87,11 @@ enum { CSA_F32 = 0, CSA_BF16 = 1, CSA_E4M3 = 2, CSA_BF16_Q_E4M3 = 3 };
  *                         kv_scale unused (may be NULL).
  * Indexer keys (CSA only, d_idx > 0): idx_key e4m3 [rows][d_idx] + idx_scale f32
  *   [rows] (E4M3) or f32 [rows][d_idx] (F32).  One key per entry, no rotation.
+ *   idx_dtype == CSA_E2M1 (FP4 indexer keys, [S]: "FP4 for the indexer"; needs
+ *   kv_dtype E4M3 and d_idx in {32, 64, 128}): idx_key u8 [rows][d_idx/2], two OCP
+ *   e2m1 codes per byte (element 2i in the low nibble, 2i+1 in the high), idx_scale
+ *   f32 [rows]; key = code * scale, scale = max|key|/6 in fp32 (1 if that is 0 or
+ *   subnormal), codes rounded to nearest even and saturated at +-6.
  * Stored entries are already rotated (partial RoPE at the block's first token).
  * win: the sliding-window ring [B][win_cap][d] in win_dtype (CSA_F32 or CSA_BF16)
  *   holding RAW (unrotated) recent tokens: token p lives in slot p % win_cap.
@@ -116,6 +121,7 @@ typedef struct csa_cache {
   void *win;
   float *pool_state;
   int64_t *n_tokens;
+  int32_t idx_dtype;    /* indexer-key storage: 0 = as kv_dtype, CSA_E2M1 = FP4 (see above) */
 } csa_cache;
 
 /* Library version (major*10000 + minor*100 + patch). */

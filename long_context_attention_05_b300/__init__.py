@@ -18,7 +18,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libcsa.so")
 
-CSA_F32, CSA_BF16, CSA_E4M3, CSA_BF16_Q_E4M3 = 0, 1, 2, 3
+CSA_F32, CSA_BF16, CSA_E4M3, CSA_BF16_Q_E4M3, CSA_E2M1 = 0, 1, 2, 3, 4
 CSA_OK = 0
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "WORKSPACE", 4: "CUDA", 5: "TIMEOUT"}
 STATUS_CODES = {v: k for k, v in STATUS_NAMES.items()}
@@ -40,6 +40,7 @@ class CsaCacheStruct(ctypes.Structure):
         ("kv_nope", ctypes.c_void_p), ("kv_scale", ctypes.c_void_p), ("kv_rope", ctypes.c_void_p),
         ("idx_key", ctypes.c_void_p), ("idx_scale", ctypes.c_void_p), ("page_table", ctypes.c_void_p),
         ("win", ctypes.c_void_p), ("pool_state", ctypes.c_void_p), ("n_tokens", ctypes.c_void_p),
+        ("idx_dtype", ctypes.c_int32),
     ]
 
 
@@ -124,12 +125,13 @@ class Cache:
     at them.  Tensor names follow include/csa.h."""
 
     def __init__(self, *, m, d, d_rope, d_idx, kv_dtype, win_dtype, n_win, win_cap, page_size=0,
-                 max_pages=0, max_entries=0, rope_theta=10000.0, tensors: Dict[str, torch.Tensor]):
+                 max_pages=0, max_entries=0, rope_theta=10000.0, tensors: Dict[str, torch.Tensor], idx_dtype=0):
         self.t = tensors
         s = CsaCacheStruct()
         s.m, s.d, s.d_rope, s.d_idx = m, d, d_rope, d_idx
         s.kv_dtype, s.win_dtype, s.n_win, s.win_cap = kv_dtype, win_dtype, n_win, win_cap
         s.page_size, s.max_pages, s.max_entries, s.rope_theta = page_size, max_pages, max_entries, rope_theta
+        s.idx_dtype = idx_dtype
         for name in ("kv_nope", "kv_scale", "kv_rope", "idx_key", "idx_scale", "page_table", "win",
                      "pool_state", "n_tokens"):
             setattr(s, name, _ptr(tensors.get(name)))
@@ -161,7 +163,8 @@ class Cache:
                    kv_dtype=CSA_E4M3 if w.kv_dtype == "e4m3" else CSA_F32,
                    win_dtype=CSA_F32 if w.tok_dtype == "f32" else CSA_BF16,
                    n_win=w.n_win, win_cap=w.win_cap, page_size=w.page_size, max_pages=w.max_pages,
-                   max_entries=w.max_entries if not w.page_size else 0, rope_theta=w.theta, tensors=t)
+                   max_entries=w.max_entries if not w.page_size else 0, rope_theta=w.theta, tensors=t,
+                   idx_dtype=CSA_E2M1 if getattr(w, "idx_dtype", "") == "e2m1" else 0)
 
 
 def to_device(a: np.ndarray, device="cuda") -> torch.Tensor:

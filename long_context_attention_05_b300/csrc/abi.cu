@@ -75,6 +75,10 @@ csa_status check_cache(const csa_cache *c) {
   if (c->kv_dtype == CSA_E4M3 && !c->kv_scale) return fail(CSA_ERR_INVALID_ARG, "kv_scale is NULL");
   if (c->d_idx > 0 && (!c->idx_key || (c->kv_dtype == CSA_E4M3 && !c->idx_scale)))
     return fail(CSA_ERR_INVALID_ARG, "indexer key pointers are NULL");
+  if (c->idx_dtype != 0 && c->idx_dtype != CSA_E2M1)
+    return fail(CSA_ERR_INVALID_ARG, "idx_dtype must be 0 (as kv_dtype) or CSA_E2M1");
+  if (c->idx_dtype == CSA_E2M1 && (c->kv_dtype != CSA_E4M3 || c->d_idx < 32))
+    return fail(CSA_ERR_UNSUPPORTED, "FP4 indexer keys need kv_dtype E4M3 and d_idx in {32, 64, 128}");
   if (!a16(c->kv_nope) || !a16(c->kv_rope) || !a16(c->win) || !a16(c->pool_state) || !a16(c->idx_key) ||
       ((uintptr_t)c->kv_scale & 3) || ((uintptr_t)c->idx_scale & 3) || ((uintptr_t)c->n_tokens & 7))
     return fail(CSA_ERR_INVALID_ARG, "cache arrays must be 16-byte aligned");
@@ -89,6 +93,7 @@ csa::CacheView view(const csa_cache *c) {
   v.kv_nope = (const uint8_t *)c->kv_nope; v.kv_scale = c->kv_scale; v.kv_rope = (const uint8_t *)c->kv_rope;
   v.idx_key = (const uint8_t *)c->idx_key; v.idx_scale = c->idx_scale; v.page_table = c->page_table;
   v.win = (const uint8_t *)c->win; v.pool_state = c->pool_state; v.n_tokens = (long long *)c->n_tokens;
+  v.idx_fp4 = c->idx_dtype == CSA_E2M1;
   return v;
 }
 
@@ -269,7 +274,7 @@ csa_cache seq_view(const csa_cache *c, int b) {
     s.kv_nope = (uint8_t *)c->kv_nope + r0 * (c->d - c->d_rope) * eb;
     s.kv_rope = (uint8_t *)c->kv_rope + r0 * c->d_rope * (c->kv_dtype == CSA_E4M3 ? 2 : 4);
     if (c->kv_scale) s.kv_scale = c->kv_scale + r0;
-    if (c->idx_key) s.idx_key = (uint8_t *)c->idx_key + r0 * c->d_idx * eb;
+    if (c->idx_key) s.idx_key = (uint8_t *)c->idx_key + r0 * (c->idx_dtype == CSA_E2M1 ? c->d_idx / 2 : c->d_idx * eb);
     if (c->idx_scale) s.idx_scale = c->idx_scale + r0;
   } else {
     s.page_table = c->page_table + (size_t)b * c->max_pages;

@@ -24,6 +24,7 @@ struct CacheView {
   const uint8_t *win;
   float *pool_state;
   long long *n_tokens;
+  int idx_fp4;            // indexer keys are packed e2m1 (two per byte) + per-entry scale
 };
 
 // Per-frequency phase increments of the rotary embedding, as 64-bit fixed-point
@@ -60,6 +61,31 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2_scaled(uint32_t v) {
 
 __device__ __forceinline__ uint8_t f32_to_e4m3_rn_sat(float x) {
   return (uint8_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
+}
+
+// e2m1 (FP4) code of x, round to nearest with ties to the even code (mantissa bit 0),
+// saturating at +-6; -0 and values that round to 0 give code 0.
+__device__ __forceinline__ uint32_t f32_to_e2m1_rn_sat(float x) {
+  const float a = fabsf(x);
+  const uint32_t m = (uint32_t)(a > 0.25f) + (uint32_t)(a >= 0.75f) + (uint32_t)(a > 1.25f) + (uint32_t)(a >= 1.75f) +
+                     (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) + (uint32_t)(a > 5.0f);
+  return m | ((x < 0.f && m) ? 8u : 0u);
+}
+
+// e2m1 code (low 4 bits) -> float
+__device__ __forceinline__ float e2m1_to_f32(uint32_t c) {
+  const float mag[8] = {0.f, 0.5f, 1.f, 1.5f, 2.f, 3.f, 4.f, 6.f};
+  const float v = mag[c & 7u];
+  return (c & 8u) ? -v : v;
+}
+
+// Eight packed e2m1 codes (a 32-bit word, code k in bits 4k..4k+3) -> eight e4m3 codes
+// of the same values (exact: every e2m1 value is an e4m3 value), bytes k of {lo, hi}.
+__device__ __forceinline__ void e2m1x8_to_e4m3x8(uint32_t w, uint32_t &lo, uint32_t &hi) {
+  constexpr uint32_t kMagLo = 0x3C383000u, kMagHi = 0x4C484440u;   // e4m3 of 0, .5, 1, 1.5 | 2, 3, 4, 6
+  const uint32_t s = (w >> 3) & 0x11111111u;                        // sign of each code, one bit per nibble
+  lo = __byte_perm(kMagLo, kMagHi, w & 0x7777u) | __byte_perm(0x8000u, 0u, s & 0xFFFFu);
+  hi = __byte_perm(kMagLo, kMagHi, (w >> 16) & 0x7777u) | __byte_perm(0x8000u, 0u, s >> 16);
 }
 
 __device__ __forceinline__ uint16_t f32_to_bf16_rn(float x) {

@@ -116,7 +116,7 @@ __device__ void pool_block(const CompressArgs &a, int b, long long n0, long long
   if (c.kv_dtype == CSA_E4M3) {
     const float amax_kv = block_max((kv && ch < rope0) ? fabsf(e) : 0.f, red);
     const float amax_ix = block_max((active && !kv) ? fabsf(e) : 0.f, red);
-    float s_kv = amax_kv / 448.0f, s_ix = amax_ix / 448.0f;
+    float s_kv = amax_kv / 448.0f, s_ix = amax_ix / (c.idx_fp4 ? 6.0f : 448.0f);
     if (!(s_kv >= 1.17549435e-38f)) s_kv = 1.0f;
     if (!(s_ix >= 1.17549435e-38f)) s_ix = 1.0f;
     if (kv && ch < rope0) {
@@ -125,8 +125,16 @@ __device__ void pool_block(const CompressArgs &a, int b, long long n0, long long
     } else if (kv) {
       reinterpret_cast<uint16_t *>(const_cast<uint8_t *>(c.kv_rope))[row * c.d_rope + (ch - rope0)] =
           f32_to_bf16_rn(e);
-    } else if (active) {
+    } else if (active && !c.idx_fp4) {
       const_cast<uint8_t *>(c.idx_key)[row * c.d_idx + (ch - c.d)] = f32_to_e4m3_rn_sat(e / s_ix);
+      if (ch == c.d) const_cast<float *>(c.idx_scale)[row] = s_ix;
+    }
+    if (c.idx_fp4) {   // two e2m1 codes per byte: the even channel writes its own and its neighbour's
+      const uint32_t code = (active && !kv) ? f32_to_e2m1_rn_sat(e / s_ix) : 0u;
+      const uint32_t next = __shfl_down_sync(0xffffffffu, code, 1);   // every lane takes part
+      const int k = ch - c.d;
+      if (active && !kv && (k & 1) == 0)
+        const_cast<uint8_t *>(c.idx_key)[row * (c.d_idx / 2) + k / 2] = (uint8_t)(code | (next << 4));
       if (ch == c.d) const_cast<float *>(c.idx_scale)[row] = s_ix;
     }
   } else {

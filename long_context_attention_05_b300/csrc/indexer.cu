@@ -53,7 +53,16 @@ __global__ void __launch_bounds__(256) k_index_generic(CacheView c, int n_q, con
   const long long r = entry_row(c, b, j);
   float k[DI];
   float scale = 1.f;
-  if (c.kv_dtype == CSA_E4M3) {
+  if (c.idx_fp4) {   // FP4 keys: DI/2 bytes, two e2m1 codes each
+    const uint32_t *src = reinterpret_cast<const uint32_t *>(c.idx_key + r * (DI / 2));
+#pragma unroll
+    for (int v = 0; v < DI / 8; ++v) {
+      const uint32_t wd = __ldg(src + v);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) k[v * 8 + q] = e2m1_to_f32(wd >> (4 * q));
+    }
+    scale = __ldg(c.idx_scale + r);
+  } else if (c.kv_dtype == CSA_E4M3) {
     const uint4 *src = reinterpret_cast<const uint4 *>(c.idx_key + r * DI);
 #pragma unroll
     for (int v = 0; v < DI / 16; ++v) {

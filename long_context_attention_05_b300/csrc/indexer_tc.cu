@@ -48,6 +48,12 @@ constexpr int kStageBytes = kTileM * kDI;
 constexpr int kEpiGroups = 3;   // epilogue warpgroups; group e takes tiles it % 3 == e
 constexpr int kThreads = 64 + 128 * kEpiGroups;
 constexpr int kMaxFlatRows = 256;   // the flat grid serves fewer query rows than this
+// FP4 keys: TMA brings packed rows (64 bytes per entry) into kStages raw stages of
+// 8 KB; a converter warpgroup turns each into a 16 KB e4m3 tile (the same 128-byte
+// swizzled layout TMA gives e4m3 keys) in one of kConvStages stages that the MMA
+// reads.  Both rings fit in the 128 KB the e4m3 key ring uses.
+constexpr int kConvStages = 4;
+constexpr int kRawStageBytes = kTileM * kDI / 2;
 
 struct TcArgs {
   CacheView c;
@@ -65,6 +71,7 @@ struct TcArgs {
   int starve;         // failure injection for tests: the producer issues no key copies
   int q_vec;          // q_idx is 16-byte aligned: vector loads of the query
   int hi_only;        // query-side FP8 variant: one e4m3 operand (N = heads), no lo term
+  int fp4;            // FP4 keys: raw ring + converter warpgroup (the last epilogue group)
   unsigned *hist;     // per-row histograms of score-key prefixes (kPrefixBins each), or null
 };
 
@@ -164,10 +171,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
   uint64_t *empty = full + kStages;
   uint64_t *tfull = empty + kStages;
   uint64_t *tempty = tfull + 4;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 4);
+  uint64_t *cfull = tempty + 4;    // FP4: converted tile ready (4 converter warps)
+  uint64_t *cempty = cfull + kConvStages;   // FP4: converted tile consumed (MMA commit)
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(cempty + kConvStages);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-  uint64_t *drain = tempty + 5;   // MMA drain after an abort (the 8 bytes after tmem_slot, abort_flag)
-  unsigned *shist = reinterpret_cast<unsigned *>(reinterpret_cast<uint8_t *>(tempty + 4) + 16);   // [kPrefixBins]
+  uint64_t *drain = cempty + kConvStages + 1;   // MMA drain after an abort (the 8 bytes after tmem_slot, abort_flag)
+  unsigned *shist = reinterpret_cast<unsigned *>(reinterpret_cast<uint8_t *>(cempty + kConvStages) + 16);   // [kPrefixBins]
+  // FP4: the e4m3 tiles the MMA reads are stage[0 .. kConvStages) (16 KB each); the raw
+  // packed tiles TMA writes follow them, kStages x 8 KB
+  uint8_t *raw = base + kConvStages * kStageBytes;
 
   const CacheView &c = a.c;
   // ---- work assignment.  Many query rows (>= one per SM): CTA y takes row y.
@@ -180,7 +192,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
   pdl_wait();      // n_tokens comes from the compressor just before
   pdl_trigger();
   if (threadIdx.x == 32) {   // barriers (warp 1) while warp 0 works out the partition
-    for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    // full/empty guard the TMA ring (e4m3 tiles, or FP4 raw tiles whose consumers are
+    // the 4 converter warps); cfull/cempty the converted FP4 tiles
+    for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], a.fp4 ? 4 : 1); }
+    for (int s = 0; s < kConvStages; ++s) { mbar_init(&cfull[s], 4); mbar_init(&cempty[s], 1); }
     for (int s = 0; s < 4; ++s) { mbar_init(&tfull[s], 1); mbar_init(&tempty[s], 4); }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -387,12 +402,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
         bool ok = true;
         if (lane == 0) ok = mbar_wait(&empty[s], ph ^ 1u, abort_flag, a.status, a.wait_limit);
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;   // warp-uniform
-        if (lane == 0) mbar_expect_tx(&full[s], kStageBytes);
+        // e4m3 keys: 128-byte rows straight into the MMA's tile; FP4: 64-byte packed rows
+        // into the raw ring
+        const int row_bytes = a.fp4 ? kDI / 2 : kDI;
+        uint8_t *dst = a.fp4 ? raw + s * kRawStageBytes : stage + s * kStageBytes;
+        if (lane == 0) mbar_expect_tx(&full[s], kTileM * row_bytes);
         const long long tile = tile_lo + it;
         if (c.page_size == 0) {
           if (lane == 0)
-            tma_load_2d(stage + s * kStageBytes, &kmap, &full[s], 0, (int)((long long)b * c.max_entries + tile * kTileM),
-                        policy);
+            tma_load_2d(dst, &kmap, &full[s], 0, (int)((long long)b * c.max_entries + tile * kTileM), policy);
         } else {
           for (int r0 = 0; r0 < kTileM; r0 += a.box_rows) {
             const long long j0 = tile * kTileM + r0;
@@ -408,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
             }
             const int pg = __shfl_sync(0xffffffffu, pcur, (int)(lp - pbase));
             if (lane == 0)
-              tma_load_2d(stage + s * kStageBytes + r0 * kDI, &kmap, &full[s], 0,
+              tma_load_2d(dst + r0 * row_bytes, &kmap, &full[s], 0,
                           (int)((long long)pg * c.page_size + j0 % c.page_size), policy);
           }
         }
@@ -421,20 +439,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
       const int n_mma = a.hi_only ? H : 2 * H;   // hi only, or hi | lo
       const uint32_t idesc = (1u << 4) | ((uint32_t)(n_mma >> 3) << 17) | ((uint32_t)(kTileM >> 4) << 24);
       const uint32_t bh = su32(bhi);
+      // the key tile: the TMA ring's stage (e4m3 keys) or the converted stage (FP4 keys)
+      const int n_ring = a.fp4 ? kConvStages : kStages;
+      uint64_t *tile_full = a.fp4 ? cfull : full, *tile_empty = a.fp4 ? cempty : empty;
       for (int it = 0; it < n_it; ++it) {
-        const int s = it % kStages;
-        const uint32_t ph = (uint32_t)(it / kStages) & 1u;
+        const int s = it % n_ring;
+        const uint32_t ph = (uint32_t)(it / n_ring) & 1u;
         const int acc = it % n_acc;
         const uint32_t aph = (uint32_t)(it / n_acc) & 1u;
         if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, a.status, a.wait_limit)) break;
-        if (!mbar_wait(&full[s], ph, abort_flag, a.status, a.wait_limit)) break;
+        if (!mbar_wait(&tile_full[s], ph, abort_flag, a.status, a.wait_limit)) break;
         tc_fence_after();
         const uint32_t as = su32(stage + s * kStageBytes);
         const uint32_t d = tmem + (uint32_t)(acc * 2 * H);
 #pragma unroll
         for (int kk = 0; kk < kDI / 32; ++kk)
           umma_f8(d, sw128_desc(as + kk * 32), sw128_desc(bh + kk * 32), idesc, kk > 0);
-        umma_commit(&empty[s]);
+        umma_commit(&tile_empty[s]);
         umma_commit(&tfull[acc]);
       }
     }
@@ -443,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
     // Groups take tiles in turn.  A group waits on an accumulator's next phase only
     // after finishing its previous tile, so the accumulator's previous use must be
     // older than that tile (parity waits would alias otherwise): groups <= buffers.
-    const int n_grp = min(kEpiGroups, n_acc);
+    const int n_grp = min(a.fp4 ? kEpiGroups - 1 : kEpiGroups, n_acc);   // FP4: the last group converts
     const int grp = (warp - 2) >> 2;   // epilogue group: tiles it with it % n_grp == grp
     // key scales are read four of this group's tiles ahead so their memory
     // latency overlaps the tiles in between instead of stalling each epilogue
@@ -473,6 +494,40 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
     }
     bool live = true;
     if (grp >= n_grp) live = false;
+    if (a.fp4 && grp == kEpiGroups - 1) {
+      // ---- FP4 converter: thread = entry row r of the tile.  The 64 packed bytes of the
+      //      row become its 128 e4m3 bytes, written in the 128-byte swizzle the MMA's
+      //      descriptor expects (16-byte chunk j of row r at chunk j ^ (r & 7)).
+      const int r = (warp - 2 - 4 * grp) * 32 + lane;
+      for (int it = 0; it < n_it; ++it) {
+        const int s = it % kStages, sc2 = it % kConvStages;
+        const uint32_t ph = (uint32_t)(it / kStages) & 1u, pc = (uint32_t)(it / kConvStages) & 1u;
+        bool ok = mbar_wait(&full[s], ph, abort_flag, a.status, a.wait_limit);
+        if (ok) ok = mbar_wait(&cempty[sc2], pc ^ 1u, abort_flag, a.status, a.wait_limit);
+        if (!__all_sync(0xffffffffu, ok)) break;   // warp-uniform
+        const uint4 *src = reinterpret_cast<const uint4 *>(raw + s * kRawStageBytes + r * (kDI / 2));
+        uint4 in[kDI / 32];
+#pragma unroll
+        for (int q = 0; q < kDI / 32; ++q) in[q] = src[q];
+        uint8_t *dst = stage + sc2 * kStageBytes + r * kDI;
+#pragma unroll
+        for (int q = 0; q < kDI / 32; ++q) {   // 32 codes -> two 16-byte chunks
+          uint32_t o[8];
+          e2m1x8_to_e4m3x8(in[q].x, o[0], o[1]);
+          e2m1x8_to_e4m3x8(in[q].y, o[2], o[3]);
+          e2m1x8_to_e4m3x8(in[q].z, o[4], o[5]);
+          e2m1x8_to_e4m3x8(in[q].w, o[6], o[7]);
+          *reinterpret_cast<uint4 *>(dst + (((2 * q) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4 *>(dst + (((2 * q + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic writes -> tensor-core reads
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&empty[s]);     // raw stage free for the next copy
+          mbar_arrive(&cfull[sc2]);   // converted tile ready
+        }
+      }
+    }
     for (int it0 = grp; it0 < n_it && live; it0 += 4 * n_grp) {
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -580,7 +635,7 @@ bool index_tc_supported(const CacheView &c, int heads_idx) {
 }
 
 size_t index_tc_smem_bytes() {
-  return 1024 + (size_t)kStages * kStageBytes + 2 * 128 * kDI + 128 * sizeof(float) + (2 * kStages + 8) * 8 + 16 +
+  return 1024 + (size_t)kStages * kStageBytes + 2 * 128 * kDI + 128 * sizeof(float) + (2 * kStages + 8 + 2 * kConvStages) * 8 + 16 +
          (size_t)kPrefixBins * sizeof(unsigned);
 }
 
@@ -594,12 +649,16 @@ cudaError_t launch_index_tc(const CacheView &c, int batch, int n_q, const void *
   // contiguous: the real row extent, so a tail tile past it reads zeros; paged:
   // rows are reached only through valid page ids, the extent is not known here
   const cuuint64_t rows = c.page_size == 0 ? (cuuint64_t)batch * (cuuint64_t)c.max_entries : (cuuint64_t)0x7fffffff;
-  cuuint64_t gdim[2] = {(cuuint64_t)kDI, rows};
-  cuuint64_t gstride[1] = {(cuuint64_t)kDI};
-  cuuint32_t box[2] = {(cuuint32_t)kDI, (cuuint32_t)box_rows};
+  // e4m3 keys: 128-byte rows, 128-byte swizzle (the MMA reads the tile in place);
+  // FP4 keys: 64-byte packed rows, unswizzled (the converter reads them row by row)
+  const cuuint64_t row_bytes = c.idx_fp4 ? kDI / 2 : kDI;
+  cuuint64_t gdim[2] = {row_bytes, rows};
+  cuuint64_t gstride[1] = {row_bytes};
+  cuuint32_t box[2] = {(cuuint32_t)row_bytes, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, (void *)c.idx_key, gdim, gstride, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, c.idx_fp4 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   TcArgs a;
@@ -610,6 +669,7 @@ cudaError_t launch_index_tc(const CacheView &c, int batch, int n_q, const void *
   a.starve = dbg.starve;
   a.q_vec = ((uintptr_t)q_idx & 15) == 0;
   a.hi_only = q_dtype == CSA_BF16_Q_E4M3;
+  a.fp4 = c.idx_fp4;
   if (a.hi_only) a.q_dtype = CSA_BF16;   // the input is bf16 either way
   a.hist = hist;
   const int rows_q = batch * n_q;

@@ -47,6 +47,17 @@ def to_e4m3_codes(x: np.ndarray) -> np.ndarray:
     return torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
 
 
+def to_e2m1_packed(x: np.ndarray) -> np.ndarray:
+    """float32 array [..., n] -> OCP e2m1 (FP4) codes, two per byte (element 2i in the
+    low nibble), round to nearest with ties to the even code, saturating at +-6."""
+    x = np.asarray(x, dtype=np.float32)
+    a = np.abs(x)
+    m = ((a > 0.25).astype(np.uint8) + (a >= 0.75) + (a > 1.25) + (a >= 1.75) + (a > 2.5) + (a >= 3.5) +
+         (a > 5.0)).astype(np.uint8)
+    codes = m | np.where((x < 0) & (m > 0), 8, 0).astype(np.uint8)
+    return (codes[..., 0::2] | (codes[..., 1::2] << 4)).astype(np.uint8)
+
+
 def _rng(seed: int, stream: int) -> np.random.Generator:
     return np.random.Generator(np.random.PCG64([int(seed), int(stream)]))
 
@@ -95,6 +106,7 @@ class Workload:
     extra_entries: int = 64     # spare entry capacity per sequence for repeated steps
     spare_pages: int = 0        # spare physical pages in the pool (paged caches)
     q_fp8: bool = False         # indexer: query-side FP8 variant
+    idx_dtype: str = ""         # indexer-key storage: "" (as kv_dtype) or "e2m1" (FP4)
 
     def __post_init__(self):
         if len(self.ctx) != self.batch:
@@ -299,7 +311,12 @@ def seeded_cache(w: Workload, q_idx: Optional[np.ndarray] = None, w_idx: Optiona
                 js = _rng(w.seed, _S_PLANT + 1000 * b).choice(n_e, size=n_plant, replace=False)
                 prow = _rows_of(w, page_table, b, js)
                 keys[prow] += np.float32(3.0) * dirv[None, :]
-        if w.kv_dtype == "e4m3":
+        if w.idx_dtype == "e2m1":
+            # per-entry scale in [0.6, 1.2): keys ~N(0,1) land mostly inside e2m1's +-6
+            iscale = (np.float32(0.6) * (1.0 + uniform(w.seed, _S_IS, (rows,)))).astype(np.float32)
+            out["idx_key"] = to_e2m1_packed(keys / iscale[:, None])
+            out["idx_scale"] = iscale
+        elif w.kv_dtype == "e4m3":
             iscale = _random_scales(w.seed, _S_IS, (rows,))
             out["idx_key"] = to_e4m3_codes(keys / iscale[:, None])
             out["idx_scale"] = iscale
@@ -324,7 +341,7 @@ def empty_cache(w: Workload) -> Dict[str, np.ndarray]:
         out["kv_scale"] = np.zeros((rows,), np.float32)
         out["kv_rope"] = np.zeros((rows, dr), np.uint16)
         if w.kind == "csa":
-            out["idx_key"] = np.zeros((rows, w.d_idx), np.uint8)
+            out["idx_key"] = np.zeros((rows, w.d_idx // 2 if w.idx_dtype == "e2m1" else w.d_idx), np.uint8)
             out["idx_scale"] = np.zeros((rows,), np.float32)
     else:
         out["kv_nope"] = np.zeros((rows, d - dr), np.float32)
@@ -370,5 +387,6 @@ def _bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
 
 
 def cache_bytes(arrs: Dict[str, np.ndarray]) -> int:
+    """Bytes of a cache's entry storage (KV and indexer keys with their scales)."""
     keys = ("kv_nope", "kv_scale", "kv_rope", "idx_key", "idx_scale")
     return int(sum(arrs[k].nbytes for k in keys if k in arrs))

@@ -107,6 +107,55 @@ def encode_e4m3(x: np.ndarray) -> np.ndarray:
     return np.where(nan, np.uint8(0x7F), codes).astype(np.uint8)
 
 
+E2M1_MAX = 6.0
+
+
+def _e2m1_value(code: int) -> float:
+    """Value of one OCP e2m1 (FP4) code: sign, 2 exponent bits (bias 1), 1 mantissa
+    bit; exponent 0 is subnormal (m/2); no infinity or NaN."""
+    s = -1.0 if code & 0x8 else 1.0
+    e = (code >> 1) & 0x3
+    m = code & 0x1
+    if e == 0:
+        return s * m * 0.5
+    return s * (1.0 + m / 2.0) * 2.0 ** (e - 1)
+
+
+E2M1_TABLE = np.array([_e2m1_value(c) for c in range(16)], dtype=np.float64)
+
+
+def decode_e2m1(codes: np.ndarray) -> np.ndarray:
+    return E2M1_TABLE[np.asarray(codes, dtype=np.uint8) & 0xF]
+
+
+def encode_e2m1(x: np.ndarray) -> np.ndarray:
+    """float64 -> e2m1 codes (0..15): round to nearest, ties to the even code (the one
+    with mantissa bit 0), saturating at +-6."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.minimum(np.abs(x), E2M1_MAX)
+    mags = E2M1_TABLE[:8]
+    dist = np.abs(a[..., None] - mags)                      # distance to each magnitude
+    best = dist.min(axis=-1, keepdims=True)
+    cand = dist == best                                     # one, or two at a midpoint
+    even = cand & ((np.arange(8) & 1) == 0)
+    code = np.where(even.any(axis=-1), np.argmax(even, axis=-1), np.argmax(cand, axis=-1)).astype(np.uint8)
+    return (code | np.where(np.signbit(x) & (code > 0), 0x8, 0)).astype(np.uint8)
+
+
+def unpack_e2m1(packed: np.ndarray, n: int) -> np.ndarray:
+    """Two codes per byte (element 2i in the low nibble, 2i+1 in the high) -> [.., n] codes."""
+    p = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(p.shape[:-1] + (2 * p.shape[-1],), dtype=np.uint8)
+    out[..., 0::2] = p & 0xF
+    out[..., 1::2] = p >> 4
+    return out[..., :n]
+
+
+def pack_e2m1(codes: np.ndarray) -> np.ndarray:
+    c = np.asarray(codes, dtype=np.uint8)
+    return (c[..., 0::2] | (c[..., 1::2] << 4)).astype(np.uint8)
+
+
 def decode_bf16(bits: np.ndarray) -> np.ndarray:
     """bf16 bit pattern -> float64 (bf16 is the upper half of an IEEE binary32)."""
     b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
@@ -173,6 +222,16 @@ def e4m3_scale(v: np.ndarray) -> np.float32:
     return np.float32(s)
 
 
+def e2m1_scale(v: np.ndarray) -> np.float32:
+    """FP4 indexer keys: s = fp32(max|v|) / 6 in fp32 arithmetic; 1 if that is zero
+    or below the smallest normal fp32 (the e4m3 rule with e2m1's largest value)."""
+    amax = np.float32(np.max(np.abs(v))) if v.size else np.float32(0)
+    s = np.float32(amax) / np.float32(E2M1_MAX)
+    if not (s >= np.finfo(np.float32).tiny):
+        s = np.float32(1.0)
+    return np.float32(s)
+
+
 def quantise_e4m3(v: np.ndarray) -> Tuple[np.ndarray, np.float32]:
     """Codes = RNE_e4m3(v / s), saturating; dequantised value = code * s."""
     s = e4m3_scale(v)
@@ -207,20 +266,26 @@ def compress_entries(x: np.ndarray, g: np.ndarray, bias: np.ndarray, m: int, d_r
 
 
 def compress_index_keys(ix: np.ndarray, ig: np.ndarray, bias: np.ndarray, m: int, kv_dtype: str,
-                        first_block: int, n_blocks: int) -> Dict[str, np.ndarray]:
+                        first_block: int, n_blocks: int, idx_dtype: str = "") -> Dict[str, np.ndarray]:
     """Indexer keys: the same gated pooling on the indexer-key stream, with its own
-    gate logits and bias; no rotation; e4m3 + per-entry scale (or fp32)."""
+    gate logits and bias; no rotation; e4m3 + per-entry scale (or fp32).  With
+    idx_dtype "e2m1" (FP4 indexer keys, [S]: "FP4 for the indexer"): codes
+    RNE_e2m1(e / s), s = max|e| / 6, two codes per byte."""
     keys, scale = [], []
     for j in range(first_block, first_block + n_blocks):
         e = pool_block(ix[j * m:(j + 1) * m], ig[j * m:(j + 1) * m], bias)
-        if kv_dtype == "e4m3":
+        if idx_dtype == "e2m1":
+            s = e2m1_scale(e)
+            keys.append(pack_e2m1(encode_e2m1(e / np.float64(s))))
+            scale.append(s)
+        elif kv_dtype == "e4m3":
             c, s = quantise_e4m3(e)
             keys.append(c)
             scale.append(s)
         else:
             keys.append(fp32(e))
-    out = {"idx_key": np.array(keys).reshape(n_blocks, ix.shape[1])}
-    if kv_dtype == "e4m3":
+    out = {"idx_key": np.array(keys).reshape(n_blocks, -1)}
+    if kv_dtype == "e4m3" or idx_dtype == "e2m1":
         out["idx_scale"] = np.array(scale, dtype=np.float32)
     return out
 
@@ -244,7 +309,10 @@ def decode_kv(nope: np.ndarray, scale: Optional[np.ndarray], rp: np.ndarray, kv_
     return np.concatenate([np.asarray(nope, np.float64), np.asarray(rp, np.float64)], axis=1)
 
 
-def decode_index_keys(keys: np.ndarray, scale: Optional[np.ndarray], kv_dtype: str) -> np.ndarray:
+def decode_index_keys(keys: np.ndarray, scale: Optional[np.ndarray], kv_dtype: str, idx_dtype: str = "",
+                      d_idx: int = 0) -> np.ndarray:
+    if idx_dtype == "e2m1":
+        return decode_e2m1(unpack_e2m1(keys, d_idx)) * np.asarray(scale, np.float64)[:, None]
     if kv_dtype == "e4m3":
         return decode_e4m3(keys) * np.asarray(scale, np.float64)[:, None]
     return np.asarray(keys, np.float64)

@@ -34,8 +34,8 @@ def seq_entries(w, arrs, b, n):
 
 def seq_index_keys(w, arrs, b, n):
     rows = O.entry_rows(n, b, w.max_entries, arrs.get("page_table"), w.page_size)
-    sc = arrs["idx_scale"][rows] if w.kv_dtype == "e4m3" else None
-    return O.decode_index_keys(arrs["idx_key"][rows], sc, w.kv_dtype)
+    sc = arrs["idx_scale"][rows] if (w.kv_dtype == "e4m3" or w.idx_dtype == "e2m1") else None
+    return O.decode_index_keys(arrs["idx_key"][rows], sc, w.kv_dtype, w.idx_dtype, w.d_idx)
 
 
 def new_entries(w, inp, b, ctx):
@@ -53,8 +53,8 @@ def new_entries(w, inp, b, ctx):
     if w.kind == "csa":
         ix = _dec_tok(inp["idx_x"][b], w)
         ig = _dec_tok(inp["idx_gate"][b], w)
-        ks = O.compress_index_keys(ix, ig, inp["idx_pos_bias"], w.m, w.kv_dtype, 0, nb)
-        keys = O.decode_index_keys(ks["idx_key"], ks.get("idx_scale"), w.kv_dtype)
+        ks = O.compress_index_keys(ix, ig, inp["idx_pos_bias"], w.m, w.kv_dtype, 0, nb, idx_dtype=w.idx_dtype)
+        keys = O.decode_index_keys(ks["idx_key"], ks.get("idx_scale"), w.kv_dtype, w.idx_dtype, w.d_idx)
     return ent, keys, st
 
 
@@ -141,11 +141,16 @@ def score_slack(w, q_idx, w_idx, keys, n_old, n_vis):
         return slack
     k = keys[n_old:n_vis]
     a = np.abs(k)
-    # one e4m3 step at each element's magnitude (scale-relative), in value units
-    s = np.maximum(a.max(axis=1, keepdims=True) / 448.0, 1e-30)
-    v = a / s
-    step = np.where(v >= 2.0 ** -6, np.ldexp(1.0, (np.floor(np.log2(np.maximum(v, 2.0 ** -6))) - 3).astype(int)),
-                    2.0 ** -9) * s
+    if w.idx_dtype == "e2m1":   # one e2m1 step: 0.5 below 2, 1 below 4, 2 above (scale-relative)
+        s = np.maximum(a.max(axis=1, keepdims=True) / 6.0, 1e-30)
+        v = a / s
+        step = np.where(v < 2, 0.5, np.where(v < 4, 1.0, 2.0)) * s
+    else:
+        # one e4m3 step at each element's magnitude (scale-relative), in value units
+        s = np.maximum(a.max(axis=1, keepdims=True) / 448.0, 1e-30)
+        v = a / s
+        step = np.where(v >= 2.0 ** -6, np.ldexp(1.0, (np.floor(np.log2(np.maximum(v, 2.0 ** -6))) - 3).astype(int)),
+                        2.0 ** -9) * s
     dk = step + a * (4 * w.m + 8) * 2.0 ** -24
     slack[n_old:] = (np.abs(q_idx) @ dk.T).T @ np.abs(w_idx)
     return slack

@@ -482,3 +482,41 @@ def test_window_only_layer_brute_force_and_relation_to_hca():
     a = O.query_step("swa", q, 2, sink, ent, wf, 4, n_win, dr, theta)
     b = O.query_step("hca", q, 2, sink, ent, wf, 4, n_win, dr, theta)     # t = 2 < m - 1: no entry visible
     assert np.array_equal(a["o"], b["o"]) and np.array_equal(a["lse"], b["lse"])
+
+
+# ----------------------------------------------------------------------------- FP4 (e2m1) indexer keys
+def test_e2m1_codec_definition_ties_and_packing():
+    """OCP e2m1: sign, 2 exponent bits (bias 1), 1 mantissa bit, subnormal at exponent 0."""
+    assert O.E2M1_TABLE.tolist() == [0, 0.5, 1, 1.5, 2, 3, 4, 6, -0.0, -0.5, -1, -1.5, -2, -3, -4, -6]
+    for c in range(16):   # every non-zero value round-trips to its own code
+        if O.E2M1_TABLE[c] != 0:
+            assert O.encode_e2m1(np.array([O.E2M1_TABLE[c]]))[0] == c
+    # midpoints go to the code with mantissa bit 0 (even); beyond 6 saturates
+    mids = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+    assert O.decode_e2m1(O.encode_e2m1(np.array(mids))).tolist() == [0, 1, 1, 2, 2, 4, 4]
+    assert O.encode_e2m1(np.array([7.0, -100.0, 0.26, -0.74]))[:].tolist() == [7, 15, 1, 9]
+    # two codes per byte, element 2i in the low nibble
+    assert O.pack_e2m1(np.array([1, 2, 3, 4], np.uint8)).tolist() == [0x21, 0x43]
+    assert O.unpack_e2m1(np.array([0x21, 0x43], np.uint8), 4).tolist() == [1, 2, 3, 4]
+    assert O.e2m1_scale(np.array([-3.0, 1.0])) == np.float32(np.float32(3.0) / np.float32(6.0))
+    assert O.e2m1_scale(np.zeros(4)) == np.float32(1.0)
+
+
+def test_e2m1_encoders_agree():
+    """The oracle's encoder (nearest of the eight magnitudes, ties to the even code) and
+    the input generator's (threshold counting) are written independently; they agree."""
+    from long_context_attention_05_b300 import synthetic as S
+    x = (rng.standard_normal((64, 128)) * np.exp(rng.uniform(-3, 2.5, (64, 1)))).astype(np.float32)
+    x[0, :14] = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5, -0.25, -0.75, -5, 6, 7, 0, -0.0]
+    assert np.array_equal(S.to_e2m1_packed(x), O.pack_e2m1(O.encode_e2m1(x.astype(np.float64))))
+
+
+def test_compress_index_keys_fp4_hand_worked():
+    """One block of m = 2 with slot 1 dominant (the key is its second token):
+    key (6, -3, 1, 0.2) -> scale 6/6 = 1, codes (7, 0b1101, 2, 0), packed (0xD7, 0x02)."""
+    ix = np.array([[9, 9, 9, 9], [6, -3, 1, 0.2]], dtype=np.float64)
+    out = O.compress_index_keys(ix, np.zeros_like(ix), np.array([0.0, 60.0]), 2, "e4m3", 0, 1, idx_dtype="e2m1")
+    assert out["idx_scale"].tolist() == [1.0]
+    assert out["idx_key"][0].tolist() == [0xD7, 0x02]
+    dec = O.decode_index_keys(out["idx_key"], out["idx_scale"], "e4m3", "e2m1", 4)
+    assert dec.tolist() == [[6.0, -3.0, 1.0, 0.0]]
