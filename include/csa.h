@@ -134,7 +134,11 @@ CSA_API const char *csa_last_error(void);
  * Workspace bytes that csa_index_topk, csa_topk, csa_sparse_attend and
  * hca_attend need for `batch` sequences with `n_q` queries each, `heads` query
  * heads and top-k size `k` (k = 0 for HCA).  Alignment: 256 bytes.  The first
- * 256 bytes hold a device status word (see csa_device_status).
+ * 256 bytes hold a device status word (see csa_device_status).  For calls of at
+ * most 256 query rows with a top-k, the last bytes hold the fused call's top-k
+ * area (per-row score-prefix counts, counters and candidate lists); its contents
+ * need no initialisation (counts that do not match the scores only cost time)
+ * and calls on one workspace must be stream-ordered.
  * Returns 0 when the cache geometry is invalid.
  */
 CSA_API size_t csa_workspace_size(const csa_cache *cache, int batch, int n_q, int heads, int k);

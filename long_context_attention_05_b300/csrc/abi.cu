@@ -152,13 +152,14 @@ size_t scores_bytes(const csa_cache *c, int batch, int n_q) {
   return align256((size_t)batch * n_q * entry_cap(c) * sizeof(float));
 }
 
-// Prefix histograms of a fused index + top-k call (decode-sized calls only) sit at the
-// end of the workspace, 256-byte aligned, clear of the scores and of the attention's
-// split partials (both start after the header); csa_workspace_size reserves them.
-// 0 bytes when the call has too many rows for them.
-size_t hist_bytes(int batch, int n_q) {
+// The top-k area of a fused index + top-k call (decode-sized calls only: prefix
+// histograms and the row-split top-k's counters, slots and lists) sits at the end of
+// the workspace, 256-byte aligned, clear of the scores and of the attention's split
+// partials (both start after the header); csa_workspace_size reserves it.  0 bytes
+// when the call has too many rows for it.
+size_t area_bytes(const csa_cache *c, int batch, int n_q, int k) {
   const long long rows = (long long)batch * n_q;
-  return rows <= csa::kPrefixRowsMax ? (size_t)rows * csa::kPrefixBins * sizeof(unsigned) : 0;
+  return rows <= csa::kPrefixRowsMax ? csa::topk_area_bytes((int)rows, entry_cap(c), k) : 0;
 }
 
 csa_status check_ws(void *ws, size_t ws_bytes, size_t need) {
@@ -230,18 +231,19 @@ csa_status check_index_args(const csa_cache *c, int batch, int n_q, const void *
 
 // Indexer dispatch: the tensor-core kernel for e4m3 keys of dim 128 and 32/64/128
 // heads; the CUDA-core kernel otherwise (fp32 caches, other dims).
-// hist (may be null): per-row prefix histograms for the top-k, filled only by the
-// tensor-core indexer; *hist_used tells the caller whether they were filled
+// area (may be null): the top-k area, whose prefix histograms only the tensor-core
+// indexer fills (and whose row counters it zeroes); *hist_used tells the caller
+// whether it did
 cudaError_t launch_indexer(const csa_cache *c, int batch, int n_q, const void *q_idx, int q_dtype, const float *w,
                            int heads_idx, float *scores, long long stride, void *ws, cudaStream_t st,
-                           unsigned *hist = nullptr, bool *hist_used = nullptr) {
+                           const csa::TopkArea *area = nullptr, bool *hist_used = nullptr) {
   const csa::CacheView v = view(c);
   if (hist_used) *hist_used = false;
   if (csa::index_tc_supported(v, heads_idx)) {
-    if (hist_used) *hist_used = hist != nullptr;
+    if (hist_used) *hist_used = area != nullptr;
     const csa::IndexDebug dbg{g_wait_limit.load(), g_starve.load()};
     return csa::launch_index_tc(v, batch, n_q, q_idx, q_dtype, w, heads_idx, scores, stride, num_sms(),
-                                ws ? (int *)ws : nullptr, hist, dbg, st);
+                                ws ? (int *)ws : nullptr, area, dbg, st);
   }
   return csa::launch_index_generic(v, batch, n_q, q_idx, q_dtype, w, heads_idx, scores, stride, entry_cap(c), st);
 }
@@ -332,7 +334,7 @@ size_t csa_workspace_size(const csa_cache *c, int batch, int n_q, int heads, int
   if (k > 0) need = std::max(need, kHeader + scores_bytes(c, batch, n_q));
   const AttendPlan p = attend_plan(c, batch, n_q, heads, k > 0 ? (long long)k : entry_cap(c));
   need = std::max(need, kHeader + p.part_o_bytes + p.part_ml_bytes);
-  if (k > 0) need = ((need + 255) & ~(size_t)255) + hist_bytes(batch, n_q);
+  if (k > 0) need = ((need + 255) & ~(size_t)255) + area_bytes(c, batch, n_q, k);
   return need;
 }
 
@@ -393,15 +395,17 @@ csa_status csa_index_topk(const csa_cache *c, int batch, int n_q, const void *q_
   if ((s = check_ws(ws, ws_bytes, need))) return s;
   float *scores = (float *)((char *)ws + kHeader);
   const long long cap = entry_cap(c);
-  // prefix histograms when the workspace has room for them (sized by csa_workspace_size)
-  const size_t hb = hist_bytes(batch, n_q);
+  // the top-k area when the workspace has room for it (sized by csa_workspace_size)
+  const size_t hb = area_bytes(c, batch, n_q, k);
   const size_t ho = ws_bytes >= hb ? (ws_bytes - hb) & ~(size_t)255 : 0;
-  unsigned *hist = hb && ho >= need ? (unsigned *)((char *)ws + ho) : nullptr;
+  csa::TopkArea area;
+  const bool has_area = hb && ho >= need;
+  if (has_area) area = csa::topk_area((char *)ws + ho, batch * n_q, cap, k);
   bool used = false;
   cudaError_t e = launch_indexer(c, batch, n_q, q_idx, q_dtype, w, heads_idx, scores, cap, ws, (cudaStream_t)stream,
-                                 hist, &used);
+                                 has_area ? &area : nullptr, &used);
   if (e != cudaSuccess) return cuda_status(e, "indexer launch");
-  return cuda_status(csa::launch_topk(view(c), batch, n_q, scores, cap, k, out_idx, out_count, used ? hist : nullptr,
+  return cuda_status(csa::launch_topk(view(c), batch, n_q, scores, cap, k, out_idx, out_count, used ? &area : nullptr,
                                       num_sms(), (const int *)ws, (cudaStream_t)stream),
                      "top-k launch");
 }

@@ -73,6 +73,8 @@ struct TcArgs {
   int hi_only;        // query-side FP8 variant: one e4m3 operand (N = heads), no lo term
   int fp4;            // FP4 keys: raw ring + converter warpgroup (the last epilogue group)
   unsigned *hist;     // per-row histograms of score-key prefixes (kPrefixBins each), or null
+  unsigned *sel_ctr;  // the row-split top-k's per-row counters and digit counts, zeroed here, or null
+  int sel_ctr_words;
 };
 
 __device__ __forceinline__ uint32_t su32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -206,6 +208,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_tc(const __grid_constant_
   };
   if (a.hist)
     for (int e = threadIdx.x; e < kPrefixBins; e += kThreads) shist[e] = 0u;
+  // the top-k that follows counts its CTAs and digits per row from zero (the previous
+  // call's top-k has completed: it ran before this kernel's predecessor)
+  if (a.sel_ctr) {
+    const int cta = blockIdx.y * gridDim.x + blockIdx.x, n_cta = gridDim.x * gridDim.y;
+    for (int e = cta * kThreads + threadIdx.x; e < a.sel_ctr_words; e += n_cta * kThreads) a.sel_ctr[e] = 0u;
+  }
   if (a.ctas_per_row > 0) {
     if (threadIdx.x == 0) {
       sh_row = blockIdx.y; sh_sub = blockIdx.x; sh_cnt = a.ctas_per_row;
@@ -641,7 +649,7 @@ size_t index_tc_smem_bytes() {
 
 cudaError_t launch_index_tc(const CacheView &c, int batch, int n_q, const void *q_idx, int q_dtype, const float *w,
                             int heads_idx, float *scores, long long stride, int num_sms, int *status,
-                            unsigned *hist, const IndexDebug &dbg, cudaStream_t st) {
+                            const TopkArea *area, const IndexDebug &dbg, cudaStream_t st) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   CUtensorMap map;
@@ -671,7 +679,9 @@ cudaError_t launch_index_tc(const CacheView &c, int batch, int n_q, const void *
   a.hi_only = q_dtype == CSA_BF16_Q_E4M3;
   a.fp4 = c.idx_fp4;
   if (a.hi_only) a.q_dtype = CSA_BF16;   // the input is bf16 either way
-  a.hist = hist;
+  a.hist = area ? area->hist : nullptr;
+  a.sel_ctr = area ? area->ctr : nullptr;
+  a.sel_ctr_words = area && area->ctr ? area->rows * (4 + kDigitBins) : 0;
   const int rows_q = batch * n_q;
   a.rows = rows_q;
   a.grid_sms = num_sms;

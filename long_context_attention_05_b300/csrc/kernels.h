@@ -52,21 +52,47 @@ struct IndexDebug {
   int starve;
 };
 
+struct TopkArea;
 bool index_tc_supported(const CacheView &c, int heads_idx);
 size_t index_tc_smem_bytes();
 cudaError_t launch_index_tc(const CacheView &c, int batch, int n_q, const void *q_idx, int q_dtype, const float *w,
                             int heads_idx, float *scores, long long stride, int num_sms, int *status,
-                            unsigned *hist, const IndexDebug &dbg, cudaStream_t st);
+                            const TopkArea *area, const IndexDebug &dbg, cudaStream_t st);
 
 // Histogram of the top kPrefixBits bits of the order-preserving score keys, one per
 // query row: the tensor-core indexer fills it (when given one) while it scores, and
-// the cluster top-k reads it to find the bin of the k-th largest score, then zeroes it.
+// the top-k reads it to find the bin of the k-th largest score, then zeroes it.
 constexpr int kPrefixBits = 13;
 constexpr int kPrefixBins = 1 << kPrefixBits;
 constexpr int kPrefixRowsMax = 256;   // rows served with prefix histograms (decode-sized calls)
+constexpr int kCandMax = 4096;        // threshold-bin keys resolved without a pass over every key
+
+// Row-split top-k of a fused index + top-k call: CTA p of a row takes the row's scores
+// [p * kSplitChunk, (p + 1) * kSplitChunk).  Its working area follows the prefix
+// histograms in the workspace:
+//   ctr   [rows][4]      word 0: CTAs of the row done (the ticket)      } zeroed by the
+//   dhist [rows][2048]   next 11 bits of the keys in the threshold bin  } indexer
+//   slots [rows][parts]  per CTA: (entries listed or -1, keys above the threshold
+//                        bin, keys in it, 0);
+//   lists [rows][parts][part_cap] (index, key) entries, each CTA's in index order.
+constexpr int kSplitChunk = 8192;
+constexpr int kSplitPartsMax = 256;   // entry capacities up to 2M entries
+constexpr int kDigitBins = 2048;
+struct TopkArea {
+  unsigned *hist = nullptr;   // [rows][kPrefixBins]
+  unsigned *ctr = nullptr;    // [rows][4], followed by dhist: rows * (4 + kDigitBins) words zeroed together
+  unsigned *dhist = nullptr;  // [rows][kDigitBins]
+  int4 *slots = nullptr;      // [rows][parts]
+  uint2 *lists = nullptr;     // [rows][parts][part_cap]
+  int parts = 0, part_cap = 0, rows = 0;
+};
+// bytes of the area for `rows` rows (0 when the call has too many rows for it), and
+// its layout at `base` (256-byte aligned)
+size_t topk_area_bytes(int rows, long long n_cap, int k);
+TopkArea topk_area(void *base, int rows, long long n_cap, int k);
 
 cudaError_t launch_topk(const CacheView &c, int batch, int n_q, const float *scores, long long stride, int k,
-                        int32_t *out_idx, int32_t *out_count, unsigned *hist, int num_sms, const int *status,
+                        int32_t *out_idx, int32_t *out_count, const TopkArea *area, int num_sms, const int *status,
                         cudaStream_t st);
 
 constexpr int kHG = 16;

@@ -43,19 +43,188 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *buf, int &total)
   return (w ? buf[32 + w - 1] : 0) + x - v;
 }
 
+// block_exclusive_scan for two counts at once (one set of barriers)
+__device__ __forceinline__ int2 block_exclusive_scan2(int2 v, int2 *buf, int2 &total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int2 x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int yx = __shfl_up_sync(0xffffffffu, x.x, o), yy = __shfl_up_sync(0xffffffffu, x.y, o);
+    if (lane >= o) { x.x += yx; x.y += yy; }
+  }
+  __syncthreads();
+  if (lane == 31) buf[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int2 s = lane < (int)(blockDim.x >> 5) ? buf[lane] : make_int2(0, 0);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int yx = __shfl_up_sync(0xffffffffu, s.x, o), yy = __shfl_up_sync(0xffffffffu, s.y, o);
+      if (lane >= o) { s.x += yx; s.y += yy; }
+    }
+    buf[32 + lane] = s;   // inclusive warp-total prefix
+  }
+  __syncthreads();
+  total = buf[32 + (blockDim.x >> 5) - 1];
+  const int2 before = w ? buf[32 + w - 1] : make_int2(0, 0);
+  return make_int2(before.x + x.x - v.x, before.y + x.y - v.y);
+}
+
 // A nonzero status word (the indexer's bounded wait gave up, so the scores are
 // incomplete): the row gets count -1 and all-(-1) indices instead of a selection.
 __device__ __forceinline__ bool status_failed(const int *status) {
   return status != nullptr && *reinterpret_cast<const volatile int *>(status) != 0;
 }
 
+// Single-CTA radix select over one row's n > k scores s (k_topk_row, and the
+// row-split kernel's fallback; blockDim.x == kTopkThreads): three passes of an 11-,
+// 11- and 10-bit digit histogram find T, the k-th largest key, and how many keys
+// equal to T to take; one count pass and one write pass then emit the selection in
+// index order.  The histogram passes stream the row as 16-byte loads, 16 keys per
+// thread in flight (the passes are bound by load latency, not by arithmetic).
+__device__ void radix_select_row(const float *s, long long n, int k, int32_t *out) {
+  constexpr int kRB = 2048;   // digit bins
+  static_assert(kRB == 2 * kTopkThreads, "two bins per thread in the digit search");
+  __shared__ unsigned hist[kRB];
+  __shared__ int scan_buf[64];
+  __shared__ int2 scan_buf2[64];
+  __shared__ unsigned sh_prefix;
+  __shared__ int sh_krem;
+  const int lane = threadIdx.x & 31;
+  // [0, head) and [tail0, n) as scalars, the 16-byte aligned middle as float4s
+  const int head = (int)min(n, (long long)((4 - (((uintptr_t)s >> 2) & 3)) & 3));
+  const long long nvec = (n - head) >> 2;
+  const long long tail0 = head + 4 * nvec;
+  const float4 *sv = reinterpret_cast<const float4 *>(s + head);
+  unsigned prefix = 0, mask = 0;
+  int krem = k;
+#pragma unroll 1
+  for (int pass = 0; pass < 3; ++pass) {
+    const int shift = pass == 0 ? 21 : pass == 1 ? 10 : 0;
+    const unsigned dmask = pass == 2 ? 0x3FFu : 0x7FFu;
+    for (int e = threadIdx.x; e < kRB; e += blockDim.x) hist[e] = 0u;
+    __syncthreads();
+    // one key per lane, counted once per distinct bin in the warp (rows with few
+    // distinct keys would otherwise serialise up to 32 atomics on one word); a warp
+    // whose keys all fall in one bin adds 32 to a count it holds in registers while
+    // the bin repeats (rows of equal keys: one atomic per warp and pass)
+    unsigned run_bin = 0u, run_cnt = 0u;   // warp-uniform
+    auto add = [&](unsigned key, bool valid) {
+      const bool in = valid && (key & mask) == prefix;
+      const unsigned bin = (key >> shift) & dmask;
+      const unsigned b0 = __shfl_sync(0xffffffffu, bin, 0);
+      if (__all_sync(0xffffffffu, in && bin == b0)) {
+        if (run_cnt && b0 != run_bin) {
+          if (lane == 0) atomicAdd(&hist[run_bin], run_cnt);
+          run_cnt = 0u;
+        }
+        run_bin = b0;
+        run_cnt += 32u;
+        return;
+      }
+      const unsigned act = __ballot_sync(0xffffffffu, in);
+      if (in) {
+        const unsigned peers = __match_any_sync(act, bin);
+        if (lane == __ffs(peers) - 1) atomicAdd(&hist[bin], (unsigned)__popc(peers));
+      }
+    };
+    for (long long v0 = 0; v0 < nvec; v0 += 4LL * blockDim.x) {   // the same trip count in every thread
+      float4 f[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const long long x = v0 + (long long)q * blockDim.x + threadIdx.x;
+        f[q] = x < nvec ? __ldg(sv + x) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const bool valid = v0 + (long long)q * blockDim.x + threadIdx.x < nvec;
+        add(float_key(f[q].x), valid);
+        add(float_key(f[q].y), valid);
+        add(float_key(f[q].z), valid);
+        add(float_key(f[q].w), valid);
+      }
+    }
+    if (threadIdx.x < 32) {   // the at most 3 + 3 unaligned keys at the ends
+      const long long j = lane < head ? lane : tail0 + (lane - head);
+      const bool valid = lane < head || (j >= tail0 && j < n);
+      add(valid ? float_key(__ldg(s + j)) : 0u, valid);
+    }
+    if (lane == 0 && run_cnt) atomicAdd(&hist[run_bin], run_cnt);
+    __syncthreads();
+    // the digit of T: thread x owns bins 2047-2x and 2046-2x (descending)
+    const int b0 = kRB - 1 - 2 * (int)threadIdx.x, b1 = b0 - 1;
+    const int c0 = (int)hist[b0], c1 = (int)hist[b1];
+    int tot;
+    const int above = block_exclusive_scan(c0 + c1, scan_buf, tot);
+    if (above < krem && above + c0 + c1 >= krem) {
+      const bool first = above + c0 >= krem;
+      sh_prefix = prefix | ((unsigned)(first ? b0 : b1) << shift);
+      sh_krem = krem - (first ? above : above + c0);
+    }
+    __syncthreads();
+    prefix = sh_prefix;
+    krem = sh_krem;
+    mask |= dmask << shift;
+  }
+  // prefix = T; take all keys > T and the first krem keys == T, in index order.  One
+  // coalesced pass in rounds of 8 keys per thread (key base + q * blockDim.x + x in
+  // thread x: index order is (q, warp, lane)); ballots rank a key inside its warp, one
+  // block scan of the (q, warp) counts ranks the warps, running totals rank the rounds;
+  // the next round's keys load while this round is ranked.  A taken key's position is
+  // (keys > T before it) + min(keys == T before it, krem).
+  {
+    constexpr int kQ = 8;
+    __shared__ int2 wc[kQ * 32];
+    const int warp = threadIdx.x >> 5, nwarps = (int)blockDim.x >> 5;
+    const unsigned lt = (1u << lane) - 1u;
+    const long long step = (long long)kQ * blockDim.x;
+    long long run_gt = 0, run_eq = 0;   // keys > T and == T in earlier rounds (uniform)
+    unsigned nk[kQ];
+#pragma unroll
+    for (int q = 0; q < kQ; ++q) {
+      const long long j = (long long)q * blockDim.x + threadIdx.x;
+      nk[q] = j < n ? float_key(__ldg(s + j)) : 0u;
+    }
+    for (long long base = 0; base < n && run_gt + min(run_eq, (long long)krem) < k; base += step) {
+      unsigned kq[kQ], bg[kQ], be[kQ];
+#pragma unroll
+      for (int q = 0; q < kQ; ++q) kq[q] = nk[q];
+#pragma unroll
+      for (int q = 0; q < kQ; ++q) {   // the next round's keys
+        const long long j = base + step + (long long)q * blockDim.x + threadIdx.x;
+        nk[q] = j < n ? float_key(__ldg(s + j)) : 0u;
+      }
+#pragma unroll
+      for (int q = 0; q < kQ; ++q) {
+        const bool valid = base + (long long)q * blockDim.x + threadIdx.x < n;
+        bg[q] = __ballot_sync(0xffffffffu, valid && kq[q] > prefix);
+        be[q] = __ballot_sync(0xffffffffu, valid && kq[q] == prefix);
+        if (lane == 0) wc[q * nwarps + warp] = make_int2(__popc(bg[q]), __popc(be[q]));
+      }
+      __syncthreads();
+      const int2 v = (int)threadIdx.x < kQ * nwarps ? wc[threadIdx.x] : make_int2(0, 0);
+      int2 tot;
+      const int2 ex = block_exclusive_scan2(v, scan_buf2, tot);
+      if ((int)threadIdx.x < kQ * nwarps) wc[threadIdx.x] = ex;
+      __syncthreads();
+#pragma unroll
+      for (int q = 0; q < kQ; ++q) {
+        const int2 o = wc[q * nwarps + warp];
+        const long long gb = run_gt + o.x + __popc(bg[q] & lt), eb = run_eq + o.y + __popc(be[q] & lt);
+        const long long j = base + (long long)q * blockDim.x + threadIdx.x;
+        if ((bg[q] >> lane) & 1u) out[gb + min(eb, (long long)krem)] = (int32_t)j;
+        else if (((be[q] >> lane) & 1u) && eb < krem) out[gb + eb] = (int32_t)j;
+      }
+      run_gt += tot.x;
+      run_eq += tot.y;
+      __syncthreads();   // wc is rewritten by the next round
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kTopkThreads) k_topk_row(CacheView c, int n_q, const float *scores,
                                                            long long stride, int k, int32_t *out_idx,
                                                            int32_t *out_count, const int *status) {
-  __shared__ unsigned hist[256];
-  __shared__ int scan_buf[64];
-  __shared__ unsigned sh_prefix;
-  __shared__ int sh_krem;
   const int row = blockIdx.x;
   const int b = row / n_q, i = row % n_q;
   pdl_wait();
@@ -63,7 +232,6 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_row(CacheView c, int n_q,
   const long long t = c.n_tokens[b] - n_q + i;
   long long n = min((t + 1) / c.m, c.cap);
   if (n > stride) n = stride;
-  const float *s = scores + (long long)row * stride;
   int32_t *out = out_idx + (long long)row * k;
   const bool failed = status_failed(status);
   if (n <= k || failed) {
@@ -71,61 +239,7 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_row(CacheView c, int n_q,
     if (threadIdx.x == 0) out_count[row] = failed ? -1 : (int32_t)n;
     return;
   }
-  unsigned prefix = 0, mask = 0;
-  int krem = k;
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    for (int e = threadIdx.x; e < 256; e += blockDim.x) hist[e] = 0;
-    __syncthreads();
-    for (long long j = threadIdx.x; j < n; j += blockDim.x) {
-      const unsigned key = float_key(__ldg(s + j));
-      const bool in = (key & mask) == prefix;
-      const unsigned bin = (key >> shift) & 255u;
-      // warp-aggregated increment: lanes with the same bin add once
-      const unsigned act = __ballot_sync(__activemask(), in);
-      if (in) {
-        const unsigned peers = __match_any_sync(act, bin);
-        if ((threadIdx.x & 31) == (unsigned)(__ffs(peers) - 1)) atomicAdd(&hist[bin], __popc(peers));
-      }
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      unsigned cum = 0;
-      int digit = 0;
-      for (int dgt = 255; dgt >= 0; --dgt) {
-        if (cum + hist[dgt] >= (unsigned)krem) { digit = dgt; break; }
-        cum += hist[dgt];
-      }
-      sh_prefix = prefix | ((unsigned)digit << shift);
-      sh_krem = krem - (int)cum;
-    }
-    __syncthreads();
-    prefix = sh_prefix;
-    krem = sh_krem;
-    mask |= 255u << shift;
-    __syncthreads();
-  }
-  // prefix = T (k-th largest key); take all keys > T and the first krem keys == T
-  const long long seg = (n + blockDim.x - 1) / blockDim.x;
-  const long long lo = threadIdx.x * seg, hi = min(n, lo + seg);
-  int gt = 0, eq = 0;
-  for (long long j = lo; j < hi; ++j) {
-    const unsigned key = float_key(__ldg(s + j));
-    gt += key > prefix;
-    eq += key == prefix;
-  }
-  int tot;
-  const int eq_before = block_exclusive_scan(eq, scan_buf, tot);
-  const int take_eq = max(0, min(eq, krem - eq_before));
-  const int pos0 = block_exclusive_scan(gt + take_eq, scan_buf, tot);
-  int pos = pos0, eq_left = take_eq;
-  for (long long j = lo; j < hi; ++j) {
-    const unsigned key = float_key(__ldg(s + j));
-    if (key > prefix || (key == prefix && eq_left > 0)) {
-      if (key == prefix) --eq_left;
-      out[pos++] = (int32_t)j;
-    }
-  }
+  radix_select_row(scores + (long long)row * stride, n, k, out);
   if (threadIdx.x == 0) out_count[row] = k;
 }
 
@@ -149,7 +263,6 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_row(CacheView c, int n_q,
 // keys of the bin; the histogram is checked against the keys and zeroed for the
 // next call.
 constexpr int kBins = 2048;
-constexpr int kCandMax = 4096;   // threshold-bin keys resolved without a pass over every key
 
 __device__ __forceinline__ float key_float(unsigned key) {
   return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
@@ -677,13 +790,297 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_cluster(CacheView c, int 
   cl.barrier_wait();   // no CTA leaves while a peer may still read its shared memory
 }
 
-// Rows with few queries get a cluster of up to 16 CTAs each; many rows get one
-// CTA each.  Rows whose slice would not fit in shared memory use k_topk_row.
+// Row-split version (fused call, the indexer's prefix histograms at hand).  CTA p of a
+// row takes its scores [p * kSplitChunk, (p + 1) * kSplitChunk), one per thread per
+// slot, and no CTA waits for another:
+//   1. the histogram gives the threshold bin b* (the prefix bin of the k-th largest
+//      key); its loads, the scores' and the row length's are all in flight at once;
+//   2. the CTA lists its keys in or above b*, in index order, as (index, key) entries
+//      in its own block of the row's list, adds the next 11 bits of each key in b* to
+//      the row's digit counts, and records its counts in its slot;
+//   3. it takes a ticket; the row's last CTA (every other CTA's writes fenced before
+//      their tickets) checks the counts against the histogram, reads the digit of the
+//      k-th key from the digit counts and its last 8 bits from the listed keys of that
+//      digit, which gives T, the k-th largest key; then it writes the list in order:
+//      keys > T, then keys == T lowest index first.
+// The counts come from the keys themselves, so a histogram that does not match them,
+// or a bin with more than kCandMax keys, sends the last CTA to the single-CTA radix
+// select over the whole row: a stale histogram costs time, never correctness.  Every
+// decision is integer counting on the same data, whatever the order of arrival.
+__global__ void __launch_bounds__(kTopkThreads) k_topk_split(CacheView c, int n_q, const float *scores,
+                                                             long long stride, int k, int32_t *out_idx,
+                                                             int32_t *out_count, TopkArea area, const int *status) {
+  constexpr int kSlots = kSplitChunk / kTopkThreads;
+  constexpr int kWarps = kTopkThreads / 32;
+  constexpr int kRun = 8;   // list entries per thread in the last CTA (k + kCandMax <= kRun * kTopkThreads)
+  static_assert(kSlots * kWarps <= kTopkThreads, "one thread per (slot, warp) count in the offset scan");
+  static_assert(kPrefixBins == 8 * kTopkThreads && kDigitBins == 2 * kTopkThreads, "bins per thread");
+  static_assert(kPrefixBits + 11 + 8 == 32, "prefix, digit and last bits make up a key");
+  __shared__ int wcnt[kSlots * kWarps];          // entries per (slot, warp), then their offsets
+  __shared__ int scan_buf[64];
+  __shared__ int2 scan_buf2[64];
+  __shared__ int sh_bin, sh_above, sh_incount;   // b*, keys above b*, keys in b* (histogram)
+  __shared__ int sh_cnt[2];                      // this CTA's keys above b* and in b*
+  __shared__ int sh_last;
+  __shared__ int pos[kSplitPartsMax + 1];        // last CTA: each part's first position in the row's list
+  __shared__ int lsum[3];                        // ... sums of the parts' counts; a part without a list
+  __shared__ unsigned lhist[256];                // ... last 8 bits of the keys of the threshold digit
+  __shared__ int sh_digit, sh_kr, sh_krem;
+  __shared__ unsigned sh_T;
+  const int p = blockIdx.x, row = blockIdx.y;
+  const int b = row / n_q, i = row % n_q;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned lt = (1u << lane) - 1u;
+  pdl_wait();
+  pdl_trigger();
+  // ---- every load issued before any is needed: the row length, the status word, this
+  //      thread's 8 histogram bins (descending over threads) and its scores (up to the
+  //      row's capacity; keys past the row's length are masked below)
+  unsigned *hrow = area.hist + (long long)row * kPrefixBins;
+  const int hb = kPrefixBins - 8 * ((int)threadIdx.x + 1);
+  const long long n_tok = c.n_tokens[b];
+  const bool failed = status_failed(status);   // the same word for every CTA
+  const uint4 h0 = *reinterpret_cast<const uint4 *>(hrow + hb);
+  const uint4 h1 = *reinterpret_cast<const uint4 *>(hrow + hb + 4);
+  const long long lo = (long long)p * kSplitChunk;
+  const float *s = scores + (long long)row * stride + lo;
+  const long long lim = min((long long)kSplitChunk, stride - lo);
+  float v[kSlots];
+#pragma unroll
+  for (int q = 0; q < kSlots; ++q) {
+    const int j = q * kTopkThreads + (int)threadIdx.x;
+    v[q] = j < lim ? __ldg(s + j) : 0.f;
+  }
+  long long n = min((n_tok - n_q + i + 1) / c.m, c.cap);
+  if (n > stride) n = stride;
+  int32_t *out = out_idx + (long long)row * k;
+  auto zero_hist = [&]() {   // leave the row's histogram zeroed for the next call
+    for (int e = 4 * (int)threadIdx.x; e < kPrefixBins; e += 4 * kTopkThreads)
+      *reinterpret_cast<uint4 *>(hrow + e) = make_uint4(0u, 0u, 0u, 0u);
+  };
+  if (n <= k || failed) {   // uniform over the row's CTAs; part 0 alone answers
+    if (p == 0) {
+      for (int j = threadIdx.x; j < k; j += blockDim.x) out[j] = (j < n && !failed) ? j : -1;
+      if (threadIdx.x == 0) out_count[row] = failed ? -1 : (int32_t)n;
+      zero_hist();   // the indexer counted this row's scores all the same
+    }
+    return;
+  }
+  const int parts = (int)((n + kSplitChunk - 1) / kSplitChunk);
+  if (p >= parts) return;
+  const int len = (int)min((long long)kSplitChunk, n - lo);
+  // ---- 1. threshold bin from the histogram
+  if (threadIdx.x == 0) { sh_bin = -1; sh_cnt[0] = 0; sh_cnt[1] = 0; }
+  {
+    const unsigned cb[8] = {h1.w, h1.z, h1.y, h1.x, h0.w, h0.z, h0.y, h0.x};   // descending bins
+    int s8 = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) s8 += (int)cb[q];
+    int tot;
+    const int above = block_exclusive_scan(s8, scan_buf, tot);   // keys in higher bins
+    if ((long long)tot == n && above < k && above + s8 >= k) {
+      int cum = above;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (cum < k && cum + (int)cb[q] >= k) { sh_bin = hb + 7 - q; sh_above = cum; sh_incount = (int)cb[q]; }
+        cum += (int)cb[q];
+      }
+    }
+  }
+  __syncthreads();
+  const int bstar = sh_bin;                                   // -1: the histogram does not count n keys
+  const bool hvalid = bstar >= 0 && sh_incount <= kCandMax;   // uniform
+  int4 *slot = area.slots + (long long)row * area.parts + p;
+  // ---- 2. this CTA's list: keys in or above b*, ordered by (slot, warp, lane) = index order
+  if (hvalid) {
+    unsigned key[kSlots], bsel[kSlots];
+    int wa = 0, wi = 0;   // this warp's keys above b* and in b*
+    unsigned *drow = area.dhist + (long long)row * kDigitBins;
+#pragma unroll
+    for (int q = 0; q < kSlots; ++q) {
+      const int j = q * kTopkThreads + (int)threadIdx.x;
+      key[q] = float_key(v[q]);
+      const unsigned pre = key[q] >> (32 - kPrefixBits);
+      const bool isin = j < len && pre == (unsigned)bstar;
+      bsel[q] = __ballot_sync(0xffffffffu, j < len && pre >= (unsigned)bstar);
+      const unsigned bin_ = __ballot_sync(0xffffffffu, isin);
+      if (isin) atomicAdd(drow + ((key[q] >> 8) & (kDigitBins - 1)), 1u);
+      if (lane == 0) wcnt[q * kWarps + warp] = __popc(bsel[q]);
+      wa += __popc(bsel[q]) - __popc(bin_);
+      wi += __popc(bin_);
+    }
+    if (lane == 0 && (wa | wi)) { atomicAdd(&sh_cnt[0], wa); atomicAdd(&sh_cnt[1], wi); }
+    __syncthreads();
+    const int vcnt = (int)threadIdx.x < kSlots * kWarps ? wcnt[threadIdx.x] : 0;
+    int my_n;
+    const int ex = block_exclusive_scan(vcnt, scan_buf, my_n);
+    if ((int)threadIdx.x < kSlots * kWarps) wcnt[threadIdx.x] = ex;
+    const bool room = my_n <= area.part_cap;   // uniform
+    if (threadIdx.x == 0) *slot = make_int4(room ? my_n : -1, sh_cnt[0], sh_cnt[1], 0);
+    __syncthreads();
+    if (room) {
+      uint2 *dst = area.lists + ((long long)row * area.parts + p) * area.part_cap;
+#pragma unroll
+      for (int q = 0; q < kSlots; ++q)
+        if ((bsel[q] >> lane) & 1u)
+          dst[wcnt[q * kWarps + warp] + __popc(bsel[q] & lt)] =
+              make_uint2((unsigned)(lo + q * kTopkThreads + (int)threadIdx.x), key[q]);
+    }
+  } else if (threadIdx.x == 0) {
+    *slot = make_int4(-1, 0, 0, 0);
+  }
+  // ---- 3. ticket (the grid-sync pattern: a CTA barrier, then one thread's fence and
+  //      atomic); the row's last CTA resolves the row
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    sh_last = atomicAdd(&area.ctr[4 * row], 1u) == (unsigned)(parts - 1);
+    if (sh_last) __threadfence();
+  }
+  __syncthreads();
+  if (!sh_last) return;
+  // ---- 4. the row's last CTA: the parts' counts and the digit counts
+  if (threadIdx.x == 0) { lsum[0] = 0; lsum[1] = 0; lsum[2] = 0; sh_digit = -1; }
+  if (threadIdx.x < 256) lhist[threadIdx.x] = 0u;
+  int4 sl = make_int4(0, 0, 0, 0);
+  if ((int)threadIdx.x < parts) sl = __ldcg(area.slots + (long long)row * area.parts + threadIdx.x);
+  const unsigned *drow = area.dhist + (long long)row * kDigitBins;
+  const int d0 = kDigitBins - 1 - 2 * (int)threadIdx.x, d1 = d0 - 1;   // this thread's digits, descending
+  const int c0 = (int)__ldcg(drow + d0), c1 = (int)__ldcg(drow + d1);
+  int2 tot2;
+  const int2 ex2 = block_exclusive_scan2(make_int2(max(sl.x, 0), c0 + c1), scan_buf2, tot2);
+  if ((int)threadIdx.x < parts) {
+    pos[threadIdx.x] = ex2.x;
+    atomicAdd(&lsum[0], sl.y);
+    atomicAdd(&lsum[1], sl.z);
+    if (sl.x < 0) lsum[2] = 1;
+  }
+  if (threadIdx.x == 0) pos[parts] = tot2.x;
+  const int kin = k - sh_above;   // keys of b* to take
+  if (hvalid && ex2.y < kin && ex2.y + c0 + c1 >= kin) {
+    const bool first = ex2.y + c0 >= kin;
+    sh_digit = first ? d0 : d1;
+    sh_kr = kin - (first ? ex2.y : ex2.y + c0);
+  }
+  __syncthreads();
+  // b* is the threshold bin iff fewer than k keys lie above it and at least k in or
+  // above it; the parts' own counts decide, whatever the histogram held
+  const bool ok = hvalid && lsum[2] == 0 && lsum[0] == sh_above && lsum[1] == sh_incount && sh_digit >= 0;
+  if (!ok) {
+    radix_select_row(scores + (long long)row * stride, n, k, out);
+  } else {
+    // this thread's contiguous run of the row's list (index order), held in registers
+    const int N = tot2.x;   // < k + kCandMax <= kRun * kTopkThreads
+    const int R = (N + kTopkThreads - 1) / kTopkThreads;
+    const int x0 = min(N, (int)threadIdx.x * R), x1 = min(N, x0 + R);
+    uint2 e[kRun];
+#pragma unroll
+    for (int r = 0; r < kRun; ++r) {
+      const int x = x0 + r;
+      e[r] = make_uint2(0u, 0u);
+      if (x < x1) {
+        int a0 = 0, a1 = parts - 1;   // the part holding x: the last with pos[q] <= x
+        while (a0 < a1) {
+          const int mid = (a0 + a1 + 1) >> 1;
+          if (pos[mid] <= x) a0 = mid; else a1 = mid - 1;
+        }
+        e[r] = __ldcg(area.lists + ((long long)row * area.parts + a0) * area.part_cap + (x - pos[a0]));
+      }
+    }
+    // the last 8 bits of the k-th key, from the listed keys of its digit
+    const unsigned D = ((unsigned)bstar << 11) | (unsigned)sh_digit;
+#pragma unroll
+    for (int r = 0; r < kRun; ++r)
+      if (x0 + r < x1 && (e[r].y >> 8) == D) atomicAdd(&lhist[e[r].y & 255u], 1u);
+    __syncthreads();
+    const int kr = sh_kr;
+    const int cv = threadIdx.x < 256 ? (int)lhist[255 - threadIdx.x] : 0;
+    int tot3;
+    const int ab3 = block_exclusive_scan(cv, scan_buf, tot3);
+    if (threadIdx.x < 256 && ab3 < kr && ab3 + cv >= kr) {
+      sh_T = (D << 8) | (255u - threadIdx.x);
+      sh_krem = kr - ab3;
+    }
+    __syncthreads();
+    const unsigned T = sh_T;   // keys > T all go; krem keys == T go, lowest index first
+    const int krem = sh_krem;
+    int gt = 0, eq = 0;
+#pragma unroll
+    for (int r = 0; r < kRun; ++r)
+      if (x0 + r < x1) { gt += e[r].y > T; eq += e[r].y == T; }
+    int2 tot4;
+    const int2 ex4 = block_exclusive_scan2(make_int2(gt, eq), scan_buf2, tot4);
+    int po = ex4.x + min(ex4.y, krem), eq_seen = ex4.y;
+#pragma unroll
+    for (int r = 0; r < kRun; ++r) {
+      if (x0 + r < x1) {
+        if (e[r].y > T) {
+          out[po++] = (int32_t)e[r].x;
+        } else if (e[r].y == T) {
+          if (eq_seen < krem) out[po++] = (int32_t)e[r].x;
+          ++eq_seen;
+        }
+      }
+    }
+  }
+  if (threadIdx.x == 0) out_count[row] = k;
+  zero_hist();   // every CTA of the row read it before its ticket
+}
+
+namespace {
+size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
+long long split_parts(int rows, long long n_cap, int k) {   // 0: no row-split area
+  const long long parts = (n_cap + kSplitChunk - 1) / kSplitChunk;
+  // the last CTA holds the row's list (< k + kCandMax entries) 8 entries per thread
+  return rows >= 1 && parts >= 1 && parts <= kSplitPartsMax && k >= 1 && k + kCandMax <= 8 * kTopkThreads ? parts
+                                                                                                          : 0;
+}
+int part_cap(int k) { return k + kCandMax < kSplitChunk ? k + kCandMax : kSplitChunk; }
+}  // namespace
+
+size_t topk_area_bytes(int rows, long long n_cap, int k) {
+  if (rows < 1 || rows > kPrefixRowsMax) return 0;
+  size_t bytes = (size_t)rows * kPrefixBins * sizeof(unsigned);
+  const long long parts = split_parts(rows, n_cap, k);
+  if (parts)
+    bytes += al256((size_t)rows * (4 + kDigitBins) * sizeof(unsigned)) + al256((size_t)rows * parts * sizeof(int4)) +
+             (size_t)rows * parts * part_cap(k) * sizeof(uint2);
+  return bytes;
+}
+
+TopkArea topk_area(void *base, int rows, long long n_cap, int k) {
+  TopkArea a;
+  a.rows = rows;
+  a.hist = static_cast<unsigned *>(base);
+  const long long parts = split_parts(rows, n_cap, k);
+  if (parts) {
+    char *q = static_cast<char *>(base) + (size_t)rows * kPrefixBins * sizeof(unsigned);
+    a.ctr = reinterpret_cast<unsigned *>(q);
+    a.dhist = a.ctr + (size_t)rows * 4;
+    q += al256((size_t)rows * (4 + kDigitBins) * sizeof(unsigned));
+    a.slots = reinterpret_cast<int4 *>(q);
+    q += al256((size_t)rows * parts * sizeof(int4));
+    a.lists = reinterpret_cast<uint2 *>(q);
+    a.parts = (int)parts;
+    a.part_cap = part_cap(k);
+  }
+  return a;
+}
+
+// With the indexer's prefix histograms and a row-split area (fused calls): the row-
+// split kernel.  Otherwise rows with few queries get a cluster of up to 16 CTAs each;
+// many rows get one CTA each.  Rows whose slice would not fit in shared memory use
+// k_topk_row.
 cudaError_t launch_topk(const CacheView &c, int batch, int n_q, const float *scores, long long stride, int k,
-                        int32_t *out_idx, int32_t *out_count, unsigned *hist, int num_sms, const int *status,
+                        int32_t *out_idx, int32_t *out_count, const TopkArea *area, int num_sms, const int *status,
                         cudaStream_t st) {
   const int rows = batch * n_q;
   const long long n_cap = c.cap < stride ? c.cap : stride;
+  unsigned *hist = area ? area->hist : nullptr;
+  if (area && hist && area->parts > 0 && area->rows == rows && area->part_cap == part_cap(k) &&
+      k + kCandMax <= 8 * kTopkThreads && (long long)area->parts * kSplitChunk >= n_cap)
+    return launch_pdl(k_topk_split, dim3(area->parts, rows), dim3(kTopkThreads), 0, st, 1, c, n_q, scores, stride, k,
+                      out_idx, out_count, *area, status);
   // the row kernel does not read the indexer's prefix histograms; they are left zeroed
   // for the next call all the same
   auto row_kernel = [&]() -> cudaError_t {

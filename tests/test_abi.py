@@ -105,15 +105,25 @@ def _align256(n):
 def _expected_workspace(batch, n_q, heads, k, d=512, n_win=128, entry_cap=1000):
     """The workspace layout written out: a 256-byte header; from it, the scores of the
     indexer (rows x entry capacity) or the attention's split partials, whichever is
-    larger; then, for decode-sized calls (rows <= 256) with a top-k, per-row
-    histograms of 8192 score-key prefixes at the end."""
+    larger; then, for decode-sized calls (rows <= 256) with a top-k, the top-k area at
+    the end: per-row histograms of 8192 score-key prefixes, and the row-split top-k's
+    per-row counters (4 words) and digit counts (2048 words), per-part slots (16 bytes
+    per 8192-entry part) and per-part lists of min(8192, k + 4096) (index, key)
+    entries of 8 bytes."""
     rows = batch * n_q
     chunks = -(-(k + n_win) // 64)              # tensor-core attention: 64-key chunks
     splits = -(-chunks // 2) if n_q == 1 else 1  # decode: two chunks per split
     parts = rows * splits * heads
     part_bytes = (_align256(parts * d * 4) + _align256(parts * 2 * 4)) if splits > 1 else 0
     need = max(256 + _align256(rows * entry_cap * 4), 256 + part_bytes)
-    return _align256(need) + (rows * 8192 * 4 if rows <= 256 else 0)
+    area = 0
+    if rows <= 256:
+        tk_parts = -(-entry_cap // 8192)
+        area = rows * 8192 * 4
+        if k + 4096 <= 8192:
+            area += (_align256(rows * 2052 * 4) + _align256(rows * tk_parts * 16)
+                     + rows * tk_parts * min(8192, k + 4096) * 8)
+    return _align256(need) + area
 
 
 @pytest.mark.parametrize("batch,n_q", [(4, 1), (32, 1), (256, 1), (257, 1), (2, 300)])
@@ -130,6 +140,7 @@ def test_split_plan_does_not_depend_on_the_batch():
     the partials grow exactly linearly with the batch."""
     lib = L.lib()
     s = _struct(max_entries=10)   # tiny scores: the partials set the size
-    sizes = [lib.csa_workspace_size(ctypes.byref(s), b, 1, 64, 2048) - b * 8192 * 4 for b in (1, 2, 3, 8)]
+    area = lambda b: b * 8192 * 4 + _align256(b * 2052 * 4) + _align256(b * 16) + b * (2048 + 4096) * 8
+    sizes = [lib.csa_workspace_size(ctypes.byref(s), b, 1, 64, 2048) - area(b) for b in (1, 2, 3, 8)]
     per_row = [(sizes[i] - 256) for i in range(4)]
     assert all(abs(per_row[i] / (1, 2, 3, 8)[i] - per_row[0]) < 512 for i in range(4))

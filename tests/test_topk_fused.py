@@ -1,10 +1,10 @@
 """The fused indexer + top-k call.  When the tensor-core indexer runs, it also counts
-each query row's scores per 13-bit key prefix, and the cluster top-k finds the bin
+each query row's scores per 13-bit key prefix, and the row-split top-k finds the bin
 of the k-th largest score from those counts instead of building its own histogram.
 The selection must equal the separate calls' (same scores, exact selection either
 way), on repeated calls (the top-k leaves the counts zeroed), and when the workspace
-starts out holding garbage (counts that do not match the scores send the top-k to
-its radix passes)."""
+starts out holding garbage or counts that do not match the scores (the top-k checks
+the counts against the keys and takes its radix passes over the row instead)."""
 import numpy as np
 import pytest
 import torch
@@ -30,13 +30,33 @@ def _outs(w):
     return idx, cnt
 
 
-def _separate(w, cache, gi, ws):
+def _separate(w, cache, gi, ws, want_scores=False):
     idx, cnt = _outs(w)
     scores = torch.empty((w.batch * w.n_new, cache.entry_cap), dtype=torch.float32, device="cuda")
     L.csa_index_scores(cache, gi["q_idx"], gi["w_idx"], scores, ws)
     L.csa_topk(cache, scores, w.batch, w.n_new, w.k, idx, cnt, ws)
     torch.cuda.synchronize()
+    if want_scores:
+        return (idx.cpu().numpy(), cnt.cpu().numpy()), scores.cpu().numpy()
     return idx.cpu().numpy(), cnt.cpu().numpy()
+
+
+def _align256(n):
+    return (n + 255) // 256 * 256
+
+
+def _hist_view(w, cache, ws):
+    """The per-row prefix counts in the workspace, reached into through the layout:
+    the top-k area is the workspace's last bytes, 256-byte aligned; it starts with
+    rows x 8192 counts, then 4 counter words and 2048 digit counts per row, 16 bytes
+    per 8192-entry part and row, and min(8192, k + 4096) list entries of 8 bytes per
+    part and row."""
+    rows = w.batch * w.n_new
+    parts = -(-cache.entry_cap // 8192)
+    area = (rows * 8192 * 4 + _align256(rows * 2052 * 4) + _align256(rows * parts * 16)
+            + rows * parts * min(8192, w.k + 4096) * 8)
+    off = (ws.numel() - area) // 256 * 256
+    return ws[off:off + rows * 8192 * 4].view(torch.int32).view(rows, 8192)
 
 
 def _fused(w, cache, gi, ws):
@@ -74,19 +94,54 @@ def test_fused_with_garbage_workspace():
 def test_fused_with_counts_of_another_call():
     """Counts left in the workspace (as a fused call whose top-k never ran would leave
     them): the indexer adds the real counts on top, the total no longer equals the
-    number of scores, and the top-k builds its own histogram instead.  The layout is
-    reached into here: the counts are the last rows*8192 words of the workspace
-    (256-byte aligned)."""
+    number of scores, and the top-k selects over the whole row instead."""
     w = S.config2(ctx=(131072,) * 4)
     cache, gi, ws = _setup(w)
     ref = _separate(w, cache, gi, ws)
-    rows = w.batch * w.n_new
-    off = (ws.numel() - rows * 8192 * 4) // 256 * 256
-    hist = ws[off:off + rows * 8192 * 4].view(torch.int32)
+    hist = _hist_view(w, cache, ws)
     hist.zero_()
-    hist.view(rows, 8192)[:, 5000] = 131072 // 4   # all of each row's entries in one bin
+    hist[:, 5000] = 131072 // 4   # all of each row's entries in one bin
     _same(_fused(w, cache, gi, ws), ref, "counts of another call")
     assert int(hist.abs().sum()) == 0, "the top-k leaves the counts zeroed"
+
+
+def _prefix_counts(scores, n):
+    """Per-row counts of the top 13 bits of the order-preserving image of each score."""
+    bits = scores[:, :n].copy().view(np.uint32)
+    keys = np.where(bits & 0x80000000, ~bits, bits | 0x80000000).astype(np.uint32)
+    return np.stack([np.bincount(r >> 19, minlength=8192) for r in keys]).astype(np.int64)
+
+
+@pytest.mark.parametrize("kind", ["shifted", "overflow"])
+def test_fused_with_counts_that_total_n_but_lie(kind):
+    """Counts planted so that, once the indexer has added the real ones, each row's
+    total is exactly its number of scores but the bins are wrong.  "shifted": k
+    counts moved from the lowest bin to the highest, so the top-k's threshold bin is
+    one that holds no key.  "overflow": the threshold bin claims 100 keys near the
+    bottom of the key range while every key lies at or above it, so each CTA's list
+    outgrows its block.  The CTAs' own counts disagree with the histogram either
+    way: the selection must still be exact and the counts left zeroed."""
+    w = S.config2(ctx=(131072,) * 4)
+    cache, gi, ws = _setup(w)
+    ref, scores = _separate(w, cache, gi, ws, want_scores=True)
+    n = 131072 // 4
+    true = _prefix_counts(scores, n)
+    if kind == "shifted":
+        want = true.copy()
+        want[:, 8191] += w.k
+        want[:, 0] -= w.k
+    else:
+        assert true[:, :2].sum() == 0   # every key's prefix is at least 2
+        want = np.zeros_like(true)
+        want[:, 2] = w.k - 1
+        want[:, 1] = 100
+        want[:, 0] = n - (w.k - 1) - 100
+    planted = ((want - true) & 0xFFFFFFFF).astype(np.uint32).view(np.int32)
+    hist = _hist_view(w, cache, ws)
+    hist.copy_(torch.from_numpy(planted))
+    _same(_fused(w, cache, gi, ws), ref, f"counts that lie ({kind})")
+    assert int(hist.abs().sum()) == 0, "the top-k leaves the counts zeroed"
+    _same(_fused(w, cache, gi, ws), ref, f"call after counts that lie ({kind})")
 
 
 def test_fused_paged_ragged_stack_layer():
