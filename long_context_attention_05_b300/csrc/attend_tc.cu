@@ -114,6 +114,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_attend_tc(AttendArgs a) {
   static_assert(NT % 2 == 0, "value n-tiles in pairs");
 
   extern __shared__ __align__(16) uint8_t smem[];
+  // the rotary phase steps, read by every thread with its own pair index: from shared
+  // memory (a lane-varying index into the kernel parameters serialises its loads)
+  __shared__ unsigned long long rstep[32];
   __half *Qs = reinterpret_cast<__half *>(smem);                       // [16][LDQ]
   __half *Ks = Qs + kTcHeads * LDQ;                                          // [64][LDQ]
   float *Sf = reinterpret_cast<float *>(Ks + kKeys * LDQ);             // [16][LDS]
@@ -129,8 +132,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_attend_tc(AttendArgs a) {
   int *f_n = reinterpret_cast<int *>(c_r + kTcHeads);                        // [16] exponent of the e4m3-dim accumulator
   int *f_r = f_n + kTcHeads;                                                 // [16] ... of the rotary-dim accumulator
   long long *ksrc = reinterpret_cast<long long *>(f_r + kTcHeads);          // [64]
-  long long *ktau = ksrc + kKeys;                                       // [64] window token position
-  float2 *qcs = reinterpret_cast<float2 *>(ktau + kKeys);              // [32] (cos, sin) at t
+  float2 *qcs = reinterpret_cast<float2 *>(ksrc + kKeys);              // [32] (cos, sin) at t
   float2 *wcs = qcs + 32;                                               // [64][32] window tokens' (cos, sin)
 
   const CacheView &c = a.c;
@@ -164,13 +166,12 @@ __global__ void __launch_bounds__(kThreads, 2) k_attend_tc(AttendArgs a) {
   if (a.idx == nullptr && a.n_splits > 1 && (long long)split * a.keys_per_split >= U) return;   // uniform
 
   // key source of slot u of the row's key list: entry row (>= 0), -2 - ring row
-  // (window token), -1 (absent); *tau = the window token's position
-  auto key_src = [&](long long u, long long &tau, float &sn) {
+  // (window token at position t - W + 1 + u), -1 (absent)
+  auto key_src = [&](long long u, float &sn) {
     long long src = -1;
-    tau = 0;
     sn = 0.f;
     if (u < W) {
-      tau = t - W + 1 + u;
+      const long long tau = t - W + 1 + u;
       if (tau >= 0) src = -2 - ((long long)b * c.win_cap + tau % c.win_cap);
     } else if (u < U) {
       const long long e = u - W;
@@ -306,33 +307,40 @@ __global__ void __launch_bounds__(kThreads, 2) k_attend_tc(AttendArgs a) {
       sig_r[gk] = (is_e || is_w) ? pow2i(er) : 0.f;
     }
   };
-  // (cos, sin) of every rotary pair of the chunk's window tokens, over all threads
-  auto win_rope = [&]() {
+  // (cos, sin) of every rotary pair of the chunk's window tokens (slot u of the key
+  // list sits at position t - W + 1 + u).  Thread x takes pair x % 32 of keys
+  // x / 32 + KS r: the first angle is evaluated, the others follow by turning it KS
+  // positions at a time (angle addition; relative error ~1e-6, far below the f16
+  // rounding of the key operand).
+  auto win_rope = [&](long long u0) {
+    constexpr int KS = kThreads / 32;
+    const int kk0 = tid >> 5, pr = tid & 31;
+    float c0, s0, cd, sd;
+    rope_cos_sin(t - W + 1 + u0 + kk0, rstep[pr], c0, s0);
+    rope_cos_sin(KS, rstep[pr], cd, sd);
 #pragma unroll
-    for (int r = 0; r < kKeys * 32 / kThreads; ++r) {
-      const int e = tid + r * kThreads, kk = e >> 5, pr = e & 31;
-      if (ksrc[kk] <= -2) {
-        float cs, sn;
-        rope_cos_sin(ktau[kk], a.rope.step[pr], cs, sn);
-        wcs[e] = make_float2(cs, sn);
-      }
+    for (int r = 0; r < kKeys / KS; ++r) {
+      const int kk = kk0 + KS * r;
+      if (ksrc[kk] <= -2) wcs[kk * 32 + pr] = make_float2(c0, s0);
+      const float c1 = fmaf(c0, cd, -s0 * sd);
+      s0 = fmaf(s0, cd, c0 * sd);
+      c0 = c1;
     }
   };
 
   const long long ch0 = (long long)split * a.chunks_per_split;
   // ---- prologue: the first chunk's key lookups, the query's rotary table
-  long long src_next = -1, tau_next = 0;
+  long long src_next = -1;
   float sn_next = 0.f;
   if (tid < kKeys) {
-    long long tau;
     float sn;
-    const long long src = key_src(ch0 * kKeys + tid, tau, sn);
+    const long long src = key_src(ch0 * kKeys + tid, sn);
     ksrc[tid] = src;
-    ktau[tid] = tau;
     sig_n[tid] = sn;
-    if (a.chunks_per_split > 1) src_next = key_src((ch0 + 1) * kKeys + tid, tau_next, sn_next);
+    if (a.chunks_per_split > 1) src_next = key_src((ch0 + 1) * kKeys + tid, sn_next);
   } else if (tid < kKeys + 32) {
     float cs, sn;
+    rstep[tid - kKeys] = a.rope.step[tid - kKeys];
     rope_cos_sin(t, a.rope.step[tid - kKeys], cs, sn);
     qcs[tid - kKeys] = make_float2(cs, sn);
   }
@@ -342,11 +350,11 @@ __global__ void __launch_bounds__(kThreads, 2) k_attend_tc(AttendArgs a) {
     f_n[tid] = kNoExp;
     f_r[tid] = kNoExp;
   }
-  __syncthreads();   // ksrc, ktau, qcs
+  __syncthreads();   // ksrc, qcs, rstep
   uint4 gbuf[NBUF];
   gather_load(gbuf);
   const bool win0 = ch0 * kKeys < W;   // uniform: window tokens in the first chunk
-  if (win0) win_rope();
+  if (win0) win_rope(ch0 * kKeys);
   {   // ---- query: rotate, scale by a power of two per head, convert to f16
     float v[QPER];
     if (a.q_dtype == CSA_BF16) {
@@ -406,15 +414,14 @@ __global__ void __launch_bounds__(kThreads, 2) k_attend_tc(AttendArgs a) {
     if (chunk != ch0) {
       if (tid < kKeys) {
         ksrc[tid] = src_next;
-        ktau[tid] = tau_next;
         sig_n[tid] = sn_next;
         src_next = -1;
-        if (chunk + 1 < ch0 + a.chunks_per_split) src_next = key_src(u0 + kKeys + tid, tau_next, sn_next);
+        if (chunk + 1 < ch0 + a.chunks_per_split) src_next = key_src(u0 + kKeys + tid, sn_next);
       }
       __syncthreads();
       gather_load(gbuf);
       if (u0 < W) {   // uniform
-        win_rope();
+        win_rope(u0);
         __syncthreads();
       }
       gather_store(gbuf);
@@ -592,7 +599,7 @@ bool attend_tc_supported(const CacheView &c, int heads, int q_dtype) {
 
 size_t attend_tc_smem_bytes(int d) {
   return (size_t)(kTcHeads + kKeys) * (d + kPadH) * 2 + (size_t)kTcHeads * (kKeys + 4) * 4 + (size_t)2 * kTcHeads * (kKeys + kPadH) * 2 +
-         (size_t)2 * kKeys * 4 + (size_t)7 * kTcHeads * 4 + (size_t)2 * kKeys * 8 + 32 * 8 + (size_t)kKeys * 32 * 8;
+         (size_t)2 * kKeys * 4 + (size_t)7 * kTcHeads * 4 + (size_t)kKeys * 8 + 32 * 8 + (size_t)kKeys * 32 * 8;
 }
 
 cudaError_t launch_attend_tc(const AttendArgs &a, int rows, cudaStream_t st) {
