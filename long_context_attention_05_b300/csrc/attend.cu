@@ -229,6 +229,16 @@ __global__ void __launch_bounds__(kCombThreads) k_attend_combine(AttendArgs a) {
   const long long t = a.c.n_tokens[bq] - a.n_q + iq;
   const long long U = (a.idx ? a.k : min((t + 1) / a.c.m, a.c.cap)) + a.c.n_win;
   const int S = (int)max(0LL, min((long long)SP, (U + a.keys_per_split - 1) / a.keys_per_split));
+  // this thread's first element pair of the first kPre splits' partial outputs, issued
+  // before the weights that scale them are known (every partial of a split below S is
+  // written and finite, so a zero weight takes it out exactly)
+  constexpr int kPre = 32;
+  float2 pre[kPre];
+  const bool pre_ok = hv && 2 * t2 < d;
+#pragma unroll
+  for (int q = 0; q < kPre; ++q)
+    pre[q] = pre_ok && q < S ? *reinterpret_cast<const float2 *>(a.part_o + (base + (long long)q * a.heads) * d + 2 * t2)
+                             : make_float2(0.f, 0.f);
   // per head: M and the split weights (the threads of a head are whole warps)
   float m = z;
   if (hv) {
@@ -260,7 +270,17 @@ __global__ void __launch_bounds__(kCombThreads) k_attend_combine(AttendArgs a) {
   const float *w = wts + hs * S;
   for (int e = 2 * t2; hv && e < d; e += 2 * TPH) {
     float o0 = 0.f, o1 = 0.f;
-    for (int s0 = 0; s0 < S; s0 += 16) {
+    int s_from = 0;
+    if (e == 2 * t2) {   // the preloaded splits, in split order
+#pragma unroll
+      for (int q = 0; q < kPre; ++q)
+        if (q < S) {
+          o0 = fmaf(w[q], pre[q].x, o0);
+          o1 = fmaf(w[q], pre[q].y, o1);
+        }
+      s_from = kPre;
+    }
+    for (int s0 = s_from; s0 < S; s0 += 16) {
       float2 v[16];
 #pragma unroll
       for (int q = 0; q < 16; ++q)
