@@ -137,11 +137,13 @@ struct AttendPlan {
   size_t part_o_bytes, part_ml_bytes;
 };
 
-// one_split: the prefill plan (one CTA walks all of a row's chunks) whatever n_q is
-AttendPlan attend_plan(const csa_cache *c, int batch, int n_q, int heads, long long list_cap, bool one_split = false) {
+// one_split: the prefill plan (one CTA walks all of a row's chunks) whatever n_q is;
+// dense: the key list is every visible entry (no top-k list)
+AttendPlan attend_plan(const csa_cache *c, int batch, int n_q, int heads, long long list_cap, bool one_split = false,
+                       bool dense = false) {
   AttendPlan p;
   p.tc = csa::attend_tc_supported(view(c), heads, CSA_BF16);
-  csa::attend_plan(one_split ? 2 : n_q, list_cap, c->n_win, p.tc, p.n_splits, p.cps);
+  csa::attend_plan(one_split ? 2 : n_q, list_cap, c->n_win, p.tc, dense && c->d >= 256, p.n_splits, p.cps);
   const size_t parts = (size_t)batch * n_q * p.n_splits * heads;
   p.part_o_bytes = p.n_splits > 1 ? align256(parts * c->d * sizeof(float)) : 0;
   p.part_ml_bytes = p.n_splits > 1 ? align256(parts * 2 * sizeof(float)) : 0;
@@ -195,7 +197,7 @@ csa_status attend_common(const csa_cache *c, int batch, int n_q, const void *q, 
     return fail(CSA_ERR_INVALID_ARG, "q must be 16-byte, out 8-byte, idx and out_lse 4-byte aligned");
   if (csa::attend_smem_bytes(c->d) > 227 * 1024) return fail(CSA_ERR_UNSUPPORTED, "d=%d too large", c->d);
   const long long list_cap = no_entries ? 0 : idx ? (long long)k : entry_cap(c);
-  const AttendPlan p = attend_plan(c, batch, n_q, heads, list_cap, one_split);
+  const AttendPlan p = attend_plan(c, batch, n_q, heads, list_cap, one_split, !no_entries && !idx);
   const size_t need = p.n_splits > 1 ? kHeader + p.part_o_bytes + p.part_ml_bytes : 0;
   if ((s = check_ws(ws, ws_bytes, need))) return s;
   csa::AttendArgs a;
@@ -332,7 +334,7 @@ size_t csa_workspace_size(const csa_cache *c, int batch, int n_q, int heads, int
   if (check_cache(c) || batch < 1 || n_q < 1 || heads < 1) return 0;
   size_t need = kHeader;
   if (k > 0) need = std::max(need, kHeader + scores_bytes(c, batch, n_q));
-  const AttendPlan p = attend_plan(c, batch, n_q, heads, k > 0 ? (long long)k : entry_cap(c));
+  const AttendPlan p = attend_plan(c, batch, n_q, heads, k > 0 ? (long long)k : entry_cap(c), false, k <= 0);
   need = std::max(need, kHeader + p.part_o_bytes + p.part_ml_bytes);
   if (k > 0) need = ((need + 255) & ~(size_t)255) + area_bytes(c, batch, n_q, k);
   return need;

@@ -305,15 +305,17 @@ __global__ void __launch_bounds__(kCombThreads) k_attend_combine(AttendArgs a) {
 }
 
 // Split plan shared by the launcher and the workspace sizing.  It depends only
-// on the key-list capacity and on whether the call is a decode (one query per
-// sequence), never on the batch, so a row's reduction order -- and its bits --
-// do not change with the other rows in the batch.  Decode: two 64-key chunks
-// per CTA (tensor-core kernel) or four 32-key chunks (CUDA-core kernel), merged
-// by k_attend_combine.  Prefill (many queries per sequence): one CTA walks all
+// on the key-list capacity, on whether the call is a decode (one query per
+// sequence) and on `wide` (a dense call -- every visible entry, no top-k list --
+// with d >= 256), never on the batch, so a row's reduction order -- and its bits
+// -- do not change with the other rows in the batch.  Decode: two 64-key chunks
+// per CTA (tensor-core kernel; four for wide calls, whose long key lists would
+// otherwise write d-wide partials for every 128 keys) or four 32-key chunks
+// (CUDA-core kernel), merged by k_attend_combine.  Prefill (many queries per sequence): one CTA walks all
 // chunks of its row.  The window comes first in a row's key list, so splits past
 // the last key hold only absent keys: a longer list of the same keys adds splits
 // whose partials weigh exactly zero in the merge.
-void attend_plan(int n_q, long long list_cap, int n_win, bool tc, int &n_splits, int &cps) {
+void attend_plan(int n_q, long long list_cap, int n_win, bool tc, bool wide, int &n_splits, int &cps) {
   const int keys = tc ? 64 : kKC;               // keys per chunk of the kernel that runs
   const long long chunks = (list_cap + n_win + keys - 1) / keys;
   if (n_q > 1) {
@@ -321,7 +323,7 @@ void attend_plan(int n_q, long long list_cap, int n_win, bool tc, int &n_splits,
     n_splits = 1;
     return;
   }
-  cps = tc ? 2 : 4;
+  cps = tc ? (wide ? 4 : 2) : 4;
   n_splits = (int)((chunks + cps - 1) / cps);
 }
 

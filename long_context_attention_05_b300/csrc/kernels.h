@@ -112,7 +112,7 @@ struct AttendArgs {
   float *out_lse;
   float scale;          // 1/sqrt(d)
 };
-void attend_plan(int n_q, long long list_cap, int n_win, bool tc, int &n_splits, int &cps);
+void attend_plan(int n_q, long long list_cap, int n_win, bool tc, bool wide, int &n_splits, int &cps);
 bool attend_tc_supported(const CacheView &c, int heads, int q_dtype);
 size_t attend_tc_smem_bytes(int d);
 cudaError_t launch_attend_tc(const AttendArgs &a, int rows, cudaStream_t st);

@@ -144,3 +144,19 @@ def test_split_plan_does_not_depend_on_the_batch():
     sizes = [lib.csa_workspace_size(ctypes.byref(s), b, 1, 64, 2048) - area(b) for b in (1, 2, 3, 8)]
     per_row = [(sizes[i] - 256) for i in range(4)]
     assert all(abs(per_row[i] / (1, 2, 3, 8)[i] - per_row[0]) < 512 for i in range(4))
+
+
+@pytest.mark.parametrize("d,cps", [(512, 4), (256, 4), (128, 2)])
+def test_dense_wide_decode_takes_four_chunks_per_split(d, cps):
+    """A dense decode call (every visible entry, no top-k list: k = 0) with d >= 256 puts
+    four 64-key chunks in a split, narrower dense calls two: the d-wide partials such a
+    call writes per split are what the merge reads back.  The plan depends on the call's
+    kind and the cache's d and capacity only (never the batch)."""
+    lib = L.lib()
+    s = _struct(d=d, max_entries=1000)
+    chunks = -(-(1000 + 128) // 64)
+    splits = -(-chunks // cps)
+    for batch in (1, 3):
+        parts = batch * splits * 64
+        want = 256 + _align256(parts * d * 4) + _align256(parts * 2 * 4)
+        assert lib.csa_workspace_size(ctypes.byref(s), batch, 1, 64, 0) == want
