@@ -76,15 +76,15 @@ __device__ __forceinline__ bool status_failed(const int *status) {
   return status != nullptr && *reinterpret_cast<const volatile int *>(status) != 0;
 }
 
-// Single-CTA radix select over one row's n > k scores s (k_topk_row, and the
-// row-split kernel's fallback; blockDim.x == kTopkThreads): three passes of an 11-,
+// Single-CTA radix select over one row's n > k scores s (k_topk_row with
+// kRowThreads, the row-split kernel's fallback with kTopkThreads; any block of
+// 256..1024 threads that divides 2048): three passes of an 11-,
 // 11- and 10-bit digit histogram find T, the k-th largest key, and how many keys
 // equal to T to take; one count pass and one write pass then emit the selection in
 // index order.  The histogram passes stream the row as 16-byte loads, 16 keys per
 // thread in flight (the passes are bound by load latency, not by arithmetic).
 __device__ void radix_select_row(const float *s, long long n, int k, int32_t *out) {
   constexpr int kRB = 2048;   // digit bins
-  static_assert(kRB == 2 * kTopkThreads, "two bins per thread in the digit search");
   __shared__ unsigned hist[kRB];
   __shared__ int scan_buf[64];
   __shared__ int2 scan_buf2[64];
@@ -151,15 +151,24 @@ __device__ void radix_select_row(const float *s, long long n, int k, int32_t *ou
     }
     if (lane == 0 && run_cnt) atomicAdd(&hist[run_bin], run_cnt);
     __syncthreads();
-    // the digit of T: thread x owns bins 2047-2x and 2046-2x (descending)
-    const int b0 = kRB - 1 - 2 * (int)threadIdx.x, b1 = b0 - 1;
-    const int c0 = (int)hist[b0], c1 = (int)hist[b1];
+    // the digit of T: thread x owns the bpt bins from 2047 - bpt x down (descending)
+    const int bpt = kRB / (int)blockDim.x;
+    const int top = kRB - 1 - bpt * (int)threadIdx.x;
+    int csum = 0;
+    for (int q = 0; q < bpt; ++q) csum += (int)hist[top - q];
     int tot;
-    const int above = block_exclusive_scan(c0 + c1, scan_buf, tot);
-    if (above < krem && above + c0 + c1 >= krem) {
-      const bool first = above + c0 >= krem;
-      sh_prefix = prefix | ((unsigned)(first ? b0 : b1) << shift);
-      sh_krem = krem - (first ? above : above + c0);
+    const int above = block_exclusive_scan(csum, scan_buf, tot);
+    if (above < krem && above + csum >= krem) {
+      int cum = above;
+      for (int q = 0; q < bpt; ++q) {
+        const int cq = (int)hist[top - q];
+        if (cum + cq >= krem) {
+          sh_prefix = prefix | ((unsigned)(top - q) << shift);
+          sh_krem = krem - cum;
+          break;
+        }
+        cum += cq;
+      }
     }
     __syncthreads();
     prefix = sh_prefix;
@@ -222,7 +231,11 @@ __device__ void radix_select_row(const float *s, long long n, int k, int32_t *ou
   }
 }
 
-__global__ void __launch_bounds__(kTopkThreads) k_topk_row(CacheView c, int n_q, const float *scores,
+// One query row per CTA of kRowThreads: several CTAs share an SM, so the rows'
+// load latencies overlap (the select is bound by them, not by arithmetic).
+constexpr int kRowThreads = 256;
+
+__global__ void __launch_bounds__(kRowThreads) k_topk_row(CacheView c, int n_q, const float *scores,
                                                            long long stride, int k, int32_t *out_idx,
                                                            int32_t *out_count, const int *status) {
   const int row = blockIdx.x;
@@ -1088,7 +1101,7 @@ cudaError_t launch_topk(const CacheView &c, int batch, int n_q, const float *sco
       const cudaError_t e = cudaMemsetAsync(hist, 0, (size_t)rows * kPrefixBins * sizeof(unsigned), st);
       if (e != cudaSuccess) return e;
     }
-    return launch_pdl(k_topk_row, dim3(rows), dim3(kTopkThreads), 0, st, 1, c, n_q, scores, stride, k, out_idx,
+    return launch_pdl(k_topk_row, dim3(rows), dim3(kRowThreads), 0, st, 1, c, n_q, scores, stride, k, out_idx,
                       out_count, status);
   };
   // cluster size: up to 16 CTAs per row for few rows; with many rows, halve it while
