@@ -17,6 +17,10 @@
 namespace csa {
 
 constexpr int kTopkThreads = 1024;
+// the row-split kernel's last CTA holds the row's list (fewer than k + kCandMax
+// entries) in registers, this many per thread: the kernel serves k + kCandMax <=
+// kSplitRun * kTopkThreads
+constexpr int kSplitRun = 8;
 
 __device__ __forceinline__ int block_exclusive_scan(int v, int *buf, int &total) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -825,7 +829,7 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_split(CacheView c, int n_
                                                              int32_t *out_count, TopkArea area, const int *status) {
   constexpr int kSlots = kSplitChunk / kTopkThreads;
   constexpr int kWarps = kTopkThreads / 32;
-  constexpr int kRun = 8;   // list entries per thread in the last CTA (k + kCandMax <= kRun * kTopkThreads)
+  constexpr int kRun = kSplitRun;
   static_assert(kSlots * kWarps <= kTopkThreads, "one thread per (slot, warp) count in the offset scan");
   static_assert(kPrefixBins == 8 * kTopkThreads && kDigitBins == 2 * kTopkThreads, "bins per thread");
   static_assert(kPrefixBits + 11 + 8 == 32, "prefix, digit and last bits make up a key");
@@ -1045,8 +1049,9 @@ size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
 long long split_parts(int rows, long long n_cap, int k) {   // 0: no row-split area
   const long long parts = (n_cap + kSplitChunk - 1) / kSplitChunk;
   // the last CTA holds the row's list (< k + kCandMax entries) 8 entries per thread
-  return rows >= 1 && parts >= 1 && parts <= kSplitPartsMax && k >= 1 && k + kCandMax <= 8 * kTopkThreads ? parts
-                                                                                                          : 0;
+  return rows >= 1 && parts >= 1 && parts <= kSplitPartsMax && k >= 1 && k + kCandMax <= kSplitRun * kTopkThreads
+             ? parts
+             : 0;
 }
 int part_cap(int k) { return k + kCandMax < kSplitChunk ? k + kCandMax : kSplitChunk; }
 }  // namespace
@@ -1091,7 +1096,7 @@ cudaError_t launch_topk(const CacheView &c, int batch, int n_q, const float *sco
   const long long n_cap = c.cap < stride ? c.cap : stride;
   unsigned *hist = area ? area->hist : nullptr;
   if (area && hist && area->parts > 0 && area->rows == rows && area->part_cap == part_cap(k) &&
-      k + kCandMax <= 8 * kTopkThreads && (long long)area->parts * kSplitChunk >= n_cap)
+      k + kCandMax <= kSplitRun * kTopkThreads && (long long)area->parts * kSplitChunk >= n_cap)
     return launch_pdl(k_topk_split, dim3(area->parts, rows), dim3(kTopkThreads), 0, st, 1, c, n_q, scores, stride, k,
                       out_idx, out_count, *area, status);
   // the row kernel does not read the indexer's prefix histograms; they are left zeroed
