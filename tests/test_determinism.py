@@ -48,8 +48,12 @@ def _slice_batch(w, arrs, inp, b):
     return w1, a1, i1
 
 
-def test_batch_invariance():
-    w = S.config2(ctx=(65536, 40000, 8192, 100000), extra_entries=64)
+@pytest.mark.parametrize("kind", ["csa", "hca512"])
+def test_batch_invariance(kind):
+    """A sequence's results are the same bits alone as in a batch (top-k call, and a
+    dense d = 512 call, whose splits hold four chunks)."""
+    w = (S.config2(ctx=(65536, 40000, 8192, 100000), extra_entries=64) if kind == "csa"
+         else S.config1(batch=4, ctx=(131072, 65536, 1024, 262144), d=512, extra_entries=64))
     arrs, inp = _setup(w)
     full = H.gpu_seeded_step(w, arrs, inp)
     for b in (0, 2, 3):
@@ -57,7 +61,8 @@ def test_batch_invariance():
         assert w1.max_entries == w.max_entries
         one = H.gpu_seeded_step(w1, a1, i1)
         for k in ("idx", "cnt", "o", "lse"):
-            assert np.array_equal(one[k][0], full[k][b]), (b, k)
+            if k in full and full[k] is not None:
+                assert np.array_equal(one[k][0], full[k][b]), (b, k)
 
 
 def test_paged_equals_contiguous():
@@ -108,11 +113,13 @@ def test_padded_key_list_is_bitwise_identical():
         assert np.array_equal(o, outs[0][0]) and np.array_equal(l, outs[0][1]), k
 
 
-def test_dense_rows_do_not_depend_on_the_entry_capacity():
+@pytest.mark.parametrize("d", [128, 512])
+def test_dense_rows_do_not_depend_on_the_entry_capacity(d):
     """HCA's split plan covers the cache's entry capacity; splits past a row's keys do
-    nothing, so the capacity (and the split count it gives) leaves the bits unchanged."""
+    nothing, so the capacity (and the split count it gives) leaves the bits unchanged.
+    d = 512 takes four 64-key chunks per split, d = 128 two."""
     import dataclasses
-    w = S.config1(batch=3, ctx=(131072, 65536, 1024))
+    w = S.config1(batch=3, ctx=(131072, 65536, 1024), d=d)
     arrs, inp = _setup(w)
     a = H.gpu_seeded_step(w, arrs, inp)
     w2 = dataclasses.replace(w, extra_entries=w.extra_entries + 3000)
